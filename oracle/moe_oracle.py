@@ -1,0 +1,352 @@
+"""Float64 CPU oracle for the forward pass of a sparsely-gated MoE FFN layer.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the library's product path imports,
+calls or links this module; only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg do.  It shares no code with the CUDA path.
+
+Everything here is plain NumPy in float64, written as the pages state the
+method, step by step, with no blocking, fusion or reordering:
+
+  [moe10]  "10. 混合专家 MoE：总参数与激活参数" (niuwancheng.cn)
+  [routing] the amazingdata.cn article on why routing is the hardest part of MoE
+  [lesson] "MoE为什么只激活一部分专家" (hi-bin.com lesson notes)
+  [explain] "为什么大模型参数这么多却不太慢？MoE 混合专家架构原理拆解" (wuaizhan.com)
+
+Layout conventions (nn.Linear orientation, out x in): x [T,d], w_router [E,d],
+expert e: w_gate [F,d], w_up [F,d], w_down [d,F]; shared expert likewise.
+
+Readings taken where the pages are silent (each is listed in the design doc):
+  * top-k ties go to the lower expert index; the chosen list is ordered by
+    logit descending, then index ascending;
+  * the selection key is the raw logit z (softmax and sigmoid are strictly
+    increasing in z, so the chosen set is the one the pages describe);
+  * routed_scaling_factor multiplies the routed weights only; the shared
+    expert is added with weight 1;
+  * capacity = ceil((T / E) * capacity_factor) in IEEE double; slots are
+    filled in ascending assignment id a = t*k + j (token order);
+  * a dropped assignment contributes zero and the surviving weights of that
+    token are not renormalised again; y excludes the residual.
+
+Parity pins: every function below is pinned by tests in tests/test_oracle_*.py
+against values the pages print, closed forms, brute force or invariants.
+"""
+
+from __future__ import annotations
+
+import math
+from typing import Dict, Iterable, Optional, Sequence
+
+import numpy as np
+
+
+# ---------------------------------------------------------------------------
+# Router: logits = x . W^T  ([moe10] "把一个大 FFN 换成一组小 FFN", the block
+# sketch's first line; [routing] the router's first step writes x . W_g with
+# W_g stored d x E, which is the transpose of the layout used here).
+# ---------------------------------------------------------------------------
+
+def router_logits(x: np.ndarray, w_router: np.ndarray,
+                  bias: Optional[np.ndarray] = None) -> np.ndarray:
+    """z[t,e] = sum_c x[t,c] * w_router[e,c] (+ bias[e])."""
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(w_router, dtype=np.float64)
+    z = x @ w.T
+    if bias is not None:
+        z = z + np.asarray(bias, dtype=np.float64)[None, :]
+    return z
+
+
+# ---------------------------------------------------------------------------
+# Gating scores ([moe10] "路由器怎样选专家：top-k 与两种门控"):
+#   softmax  p_i = exp(z_i) / sum_j exp(z_j)
+#   sigmoid  s_i = 1 / (1 + exp(-z_i)), each expert scored on its own
+# ---------------------------------------------------------------------------
+
+def softmax(z: np.ndarray) -> np.ndarray:
+    z = np.asarray(z, dtype=np.float64)
+    m = np.max(z, axis=-1, keepdims=True)       # shift for range only; cancels
+    ez = np.exp(z - m)
+    return ez / np.sum(ez, axis=-1, keepdims=True)
+
+
+def sigmoid(z: np.ndarray) -> np.ndarray:
+    z = np.asarray(z, dtype=np.float64)
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def gate_scores(z: np.ndarray, gate: str) -> np.ndarray:
+    if gate == "softmax":
+        return softmax(z)
+    if gate == "sigmoid":
+        return sigmoid(z)
+    raise ValueError(f"unknown gate {gate!r}")
+
+
+# ---------------------------------------------------------------------------
+# Top-k selection ([moe10] block sketch `probs.topk(k)`; [lesson] y_t sums over
+# TopK(s_t); k is num_experts_per_tok).
+# ---------------------------------------------------------------------------
+
+def topk_experts(z: np.ndarray, k: int) -> np.ndarray:
+    """idx[t, :] = the k experts with the largest logit, in descending order.
+
+    Equal logits are ordered by ascending expert index, so a tie always goes
+    to the lower index.  Implemented as the plain definition: sort the pairs
+    (-z[t,e], e) lexicographically and keep the first k.
+    """
+    z = np.asarray(z, dtype=np.float64)
+    T, E = z.shape
+    if not (1 <= k <= E):
+        raise ValueError("need 1 <= k <= E")
+    idx = np.empty((T, k), dtype=np.int64)
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-z[t, e], e))
+        idx[t] = order[:k]
+    return idx
+
+
+def topk_weights(scores: np.ndarray, idx: np.ndarray, renormalize: bool,
+                 routed_scaling_factor: float = 1.0) -> np.ndarray:
+    """Combine weights g[t,j] of the chosen experts.
+
+    With renormalisation ([moe10] top-k section: "再在两者之间归一化"; the
+    block sketch's `w / w.sum(-1)`): g_j = score_j / sum_sel score, then
+    multiplied by routed_scaling_factor (DeepSeek-V3: 2.5).  Without it
+    ([explain] "门控是怎么挑专家的": out = sum score_i * expert_i): g_j = score_j
+    (times the factor, which is 1 for the configurations that skip renorm).
+    """
+    scores = np.asarray(scores, dtype=np.float64)
+    T, k = idx.shape
+    g = np.empty((T, k), dtype=np.float64)
+    for t in range(T):
+        sel = np.array([scores[t, idx[t, j]] for j in range(k)])
+        if renormalize:
+            g[t] = sel / np.sum(sel)
+        else:
+            g[t] = sel
+    return g * routed_scaling_factor
+
+
+def mean_router_prob(scores: np.ndarray) -> np.ndarray:
+    """P_e = (1/T) sum_t score[t,e], the batch-mean router probability that
+    the load statistics use ([moe10] "辅助损失", definition of P_i)."""
+    scores = np.asarray(scores, dtype=np.float64)
+    return np.mean(scores, axis=0)
+
+
+# ---------------------------------------------------------------------------
+# Capacity and dispatch ([moe10] "负载不均：路由坍缩与丢 token": capacity =
+# tokens per batch / experts x capacity factor, 2 x 1.25 = 2.5 rounded up to 3;
+# over-capacity tokens skip the expert and ride the residual.  [routing] gives
+# the same formula and the same dropping rule.)
+# ---------------------------------------------------------------------------
+
+def expert_capacity(T: int, E: int, capacity_factor: Optional[float]) -> Optional[int]:
+    """ceil((T / E) * capacity_factor) in IEEE double; None = unlimited."""
+    if capacity_factor is None:
+        return None
+    return int(math.ceil((float(T) / float(E)) * float(capacity_factor)))
+
+
+def dispatch(idx: np.ndarray, E: int, capacity: Optional[int]) -> Dict[str, np.ndarray]:
+    """Group assignments by expert, filling slots in ascending assignment id.
+
+    Assignment a = t*k + j is token t's j-th choice.  Walking a upward, the
+    assignment takes the next free slot of its expert; once an expert holds
+    ``capacity`` assignments, later ones are dropped.  Returns
+
+      counts[e]   kept assignments of expert e (<= capacity)
+      drops[e]    dropped assignments of expert e
+      offsets     exclusive prefix sum of counts, length E + 1
+      perm[r]     assignment id held by grouped row r (r < offsets[E])
+      drop_mask[a] 1 where a was dropped
+      row_of[a]   grouped row of a, or -1 when dropped
+    """
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    A = T * k
+    flat = idx.reshape(A)
+    counts = np.zeros(E, dtype=np.int64)
+    drops = np.zeros(E, dtype=np.int64)
+    slot = np.full(A, -1, dtype=np.int64)
+    drop_mask = np.zeros(A, dtype=np.uint8)
+    for a in range(A):
+        e = int(flat[a])
+        if capacity is None or counts[e] < capacity:
+            slot[a] = counts[e]
+            counts[e] += 1
+        else:
+            drop_mask[a] = 1
+            drops[e] += 1
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + counts[e]
+    perm = np.full(A, -1, dtype=np.int64)
+    row_of = np.full(A, -1, dtype=np.int64)
+    for a in range(A):
+        if drop_mask[a] == 0:
+            r = offsets[flat[a]] + slot[a]
+            perm[r] = a
+            row_of[a] = r
+    return {"counts": counts, "drops": drops, "offsets": offsets, "perm": perm,
+            "drop_mask": drop_mask, "row_of": row_of, "slot": slot}
+
+
+# ---------------------------------------------------------------------------
+# Expert FFN: SwiGLU, gate and up d -> F, SiLU(gate) * up, down F -> d
+# ([moe10] "把一个大 FFN 换成一组小 FFN": each expert has the dense model's
+# FFN structure, 3 x d x F parameters).  SiLU(u) = u * sigmoid(u).
+# ---------------------------------------------------------------------------
+
+def silu(u: np.ndarray) -> np.ndarray:
+    u = np.asarray(u, dtype=np.float64)
+    return u * sigmoid(u)
+
+
+def swiglu_ffn(x_rows: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray,
+               w_down: np.ndarray) -> np.ndarray:
+    """E(x) = (SiLU(x W_gate^T) * (x W_up^T)) W_down^T for each row of x."""
+    x_rows = np.asarray(x_rows, dtype=np.float64)
+    g = x_rows @ np.asarray(w_gate, dtype=np.float64).T
+    u = x_rows @ np.asarray(w_up, dtype=np.float64).T
+    h = silu(g) * u
+    return h @ np.asarray(w_down, dtype=np.float64).T
+
+
+# ---------------------------------------------------------------------------
+# Routing for a whole batch.
+# ---------------------------------------------------------------------------
+
+def route(z: np.ndarray, k: int, gate: str, renormalize: bool,
+          routed_scaling_factor: float, capacity: Optional[int]) -> Dict[str, np.ndarray]:
+    """Scores, top-k, weights, mean probability and dispatch from logits z."""
+    z = np.asarray(z, dtype=np.float64)
+    E = z.shape[1]
+    scores = gate_scores(z, gate)
+    idx = topk_experts(z, k)
+    g = topk_weights(scores, idx, renormalize, routed_scaling_factor)
+    out = {"logits": z, "scores": scores, "topk_idx": idx, "topk_w": g,
+           "mean_prob": mean_router_prob(scores)}
+    out.update(dispatch(idx, E, capacity))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# The layer: y_t = sum_{i in TopK} g_{t,i} E_i(x_t)  (+ shared expert)
+# ([lesson] "Router 怎样给 Token 选专家"; [routing] output = sum g_i Expert_i(x);
+# [moe10] "细粒度专家与共享专家": the shared expert's output is added directly).
+# ---------------------------------------------------------------------------
+
+def moe_layer_forward(x: np.ndarray, w_router: np.ndarray, experts,
+                      k: int, gate: str, renormalize: bool,
+                      routed_scaling_factor: float = 1.0,
+                      capacity: Optional[int] = None,
+                      router_bias: Optional[np.ndarray] = None,
+                      shared=None,
+                      tokens: Optional[Sequence[int]] = None,
+                      logits: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """Per-expert grouped formulation (the block sketch's loop over experts).
+
+    ``experts[e]`` returns (w_gate_e, w_up_e, w_down_e) as float64 arrays and
+    is called at most once per expert.  ``shared`` is None or the shared
+    expert's (w_gate, w_up, w_down).  Routing is always computed for the
+    whole batch (capacity depends on earlier tokens); the output y is
+    computed for ``tokens`` only (default: all), in that order.  ``logits``,
+    when given, replaces x . W^T (+ bias).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    T = x.shape[0]
+    z = router_logits(x, w_router, router_bias) if logits is None else np.asarray(logits, np.float64)
+    r = route(z, k, gate, renormalize, routed_scaling_factor, capacity)
+    toks = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    pos = {int(t): i for i, t in enumerate(toks)}
+    y = np.zeros((len(toks), x.shape[1]), dtype=np.float64)
+    idx, g, drop = r["topk_idx"], r["topk_w"], r["drop_mask"].reshape(T, k)
+    E = z.shape[1]
+    for e in range(E):
+        rows, slots = [], []
+        for t in toks:
+            for j in range(k):
+                if idx[t, j] == e and drop[t, j] == 0:
+                    rows.append(int(t))
+                    slots.append(j)
+        if not rows:
+            continue
+        wg, wu, wd = experts[e]
+        out = swiglu_ffn(x[rows], wg, wu, wd)
+        for i, (t, j) in enumerate(zip(rows, slots)):
+            y[pos[t]] += g[t, j] * out[i]
+    if shared is not None:
+        y += swiglu_ffn(x[toks], *shared)
+    r["y"] = y
+    r["tokens"] = toks
+    return r
+
+
+def moe_layer_forward_token_loop(x: np.ndarray, w_router: np.ndarray, experts,
+                                 k: int, gate: str, renormalize: bool,
+                                 routed_scaling_factor: float = 1.0,
+                                 capacity: Optional[int] = None,
+                                 router_bias: Optional[np.ndarray] = None,
+                                 shared=None) -> np.ndarray:
+    """Second formulation: per token, per choice, no grouping or permutation.
+
+    Used only to cross-check ``moe_layer_forward`` on small inputs; both must
+    agree to float64 rounding.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    T, d = x.shape
+    z = router_logits(x, w_router, router_bias)
+    scores = gate_scores(z, gate)
+    idx = topk_experts(z, k)
+    g = topk_weights(scores, idx, renormalize, routed_scaling_factor)
+    E = z.shape[1]
+    taken = [0] * E
+    y = np.zeros((T, d), dtype=np.float64)
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            if capacity is not None and taken[e] >= capacity:
+                continue
+            taken[e] += 1
+            wg, wu, wd = experts[e]
+            y[t] += g[t, j] * swiglu_ffn(x[t:t + 1], wg, wu, wd)[0]
+        if shared is not None:
+            y[t] += swiglu_ffn(x[t:t + 1], *shared)[0]
+    return y
+
+
+# ---------------------------------------------------------------------------
+# Load statistics derived from the emitted counts and mean probabilities.
+# ---------------------------------------------------------------------------
+
+def load_fractions(counts: np.ndarray, drops: np.ndarray) -> np.ndarray:
+    """f_e = share of all assignments that chose expert e (kept + dropped)."""
+    load = np.asarray(counts, dtype=np.float64) + np.asarray(drops, dtype=np.float64)
+    return load / np.sum(load)
+
+
+def switch_balance_term(f: np.ndarray, P: np.ndarray) -> float:
+    """N * sum_i f_i * P_i, the part of the Switch auxiliary loss that the
+    worked example of [moe10] "辅助损失" evaluates (1.0 uniform, 4.0 collapsed)."""
+    f = np.asarray(f, dtype=np.float64)
+    P = np.asarray(P, dtype=np.float64)
+    return float(len(f) * np.sum(f * P))
+
+
+# ---------------------------------------------------------------------------
+# Parameter accounting ([moe10] "总参数和激活参数怎样算").
+# ---------------------------------------------------------------------------
+
+def moe_layer_params(d: int, E: int, F: int, F_s: int = 0, k: Optional[int] = None) -> int:
+    """Parameters of one MoE FFN layer: router E*d plus 3*d*F per expert
+    (all E experts, or only k of them for the active count) plus the shared
+    expert's 3*d*F_s."""
+    n_exp = E if k is None else k
+    return E * d + n_exp * 3 * d * F + 3 * d * F_s
+
+
+def expected_touched_experts(E: int, k: int, B: int) -> float:
+    """Expected number of distinct experts touched by B independent tokens
+    each choosing k of E uniformly ([moe10] "推理时：显存按总参数，计算按激活参数")."""
+    return E * (1.0 - (1.0 - k / E) ** B)

@@ -1,0 +1,367 @@
+"""Pins of the float64 oracle to facts fixed outside the oracle itself.
+
+Each test ties an oracle function to a value the pages print (fixtures under
+tests/golden/, each citing its section), a closed form, brute-force
+enumeration, or an invariant of the method.  No GPU is used.
+"""
+
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as O
+
+ABS3 = 5e-4  # the pages print 3 decimals
+
+
+# ---------------------------------------------------------------------------
+# Gating worked example ("路由器怎样选专家：top-k 与两种门控")
+# ---------------------------------------------------------------------------
+
+def test_worked_example_softmax(golden):
+    g = golden("moe10_gating_worked_example.json")
+    z = np.array([g["logits"]])
+    p = O.softmax(z)[0]
+    np.testing.assert_allclose(p, g["softmax"]["scores"], atol=ABS3)
+    idx = O.topk_experts(z, g["k"])
+    assert idx[0].tolist() == g["chosen"]
+    w = O.topk_weights(O.softmax(z), idx, renormalize=True)[0]
+    np.testing.assert_allclose(w, g["softmax"]["renormalized"], atol=ABS3)
+
+
+def test_worked_example_sigmoid_scaled(golden):
+    g = golden("moe10_gating_worked_example.json")
+    z = np.array([g["logits"]])
+    s = O.sigmoid(z)[0]
+    np.testing.assert_allclose(s, g["sigmoid"]["scores"], atol=ABS3)
+    idx = O.topk_experts(z, g["k"])
+    assert idx[0].tolist() == g["chosen"]
+    w1 = O.topk_weights(O.sigmoid(z), idx, renormalize=True)[0]
+    np.testing.assert_allclose(w1, g["sigmoid"]["renormalized"], atol=ABS3)
+    rsf = g["sigmoid"]["routed_scaling_factor"]
+    w = O.topk_weights(O.sigmoid(z), idx, renormalize=True, routed_scaling_factor=rsf)[0]
+    np.testing.assert_allclose(w, g["sigmoid"]["scaled"], atol=ABS3)
+    # the page: the selected weights sum to 1 (softmax) or 2.5 (DeepSeek-V3)
+    assert abs(w.sum() - 2.5) < 1e-12
+
+
+def test_top2_softmax_renorm_closed_form():
+    # renormalised top-2 softmax weight of the best expert is sigma(z1 - z2):
+    # exp(z1) / (exp(z1) + exp(z2)) = 1 / (1 + exp(z2 - z1)); independent of
+    # the other logits.
+    rng = np.random.default_rng(1)
+    z = rng.normal(size=(50, 6))
+    idx = O.topk_experts(z, 2)
+    w = O.topk_weights(O.softmax(z), idx, renormalize=True)
+    for t in range(z.shape[0]):
+        z1, z2 = z[t, idx[t, 0]], z[t, idx[t, 1]]
+        assert z1 >= z2
+        assert abs(w[t, 0] - 1.0 / (1.0 + math.exp(z2 - z1))) < 1e-14
+        assert abs(w[t].sum() - 1.0) < 1e-14
+
+
+def test_softmax_sigmoid_closed_values():
+    # sigma(ln 3) = 3/4 and sigma(-ln 3) = 1/4 exactly; softmax of [ln a_i]
+    # is a_i / sum a.
+    s = O.sigmoid(np.array([math.log(3.0), -math.log(3.0), 0.0]))
+    np.testing.assert_allclose(s, [0.75, 0.25, 0.5], rtol=1e-15)
+    a = np.array([1.0, 2.0, 3.0, 4.0])
+    np.testing.assert_allclose(O.softmax(np.log(a)[None])[0], a / 10.0, rtol=1e-14)
+    # shift invariance of softmax only holds if the max shift is exact
+    np.testing.assert_allclose(O.softmax(np.log(a)[None] + 700.0)[0], a / 10.0, rtol=1e-13)
+
+
+def test_mean_prob_sums_to_one_softmax():
+    rng = np.random.default_rng(2)
+    z = rng.normal(size=(37, 9))
+    P = O.mean_router_prob(O.softmax(z))
+    assert abs(P.sum() - 1.0) < 1e-13
+    # sigmoid means are each in (0, 1) and equal the plain column mean
+    P2 = O.mean_router_prob(O.sigmoid(z))
+    assert np.all((P2 > 0) & (P2 < 1))
+
+
+# ---------------------------------------------------------------------------
+# Top-k selection against brute force over all expert subsets
+# ---------------------------------------------------------------------------
+
+def _brute_topk(zrow, k):
+    """Best k-subset by sum of logits; among equal sums, the lexicographically
+    smallest sorted index tuple (the lowest-index tie rule)."""
+    best, best_key = None, None
+    for sub in itertools.combinations(range(len(zrow)), k):
+        key = (-sum(zrow[list(sub)]), sub)
+        if best_key is None or key < best_key:
+            best, best_key = sub, key
+    return sorted(best, key=lambda e: (-zrow[e], e))
+
+
+@pytest.mark.parametrize("E,k", [(4, 2), (8, 2), (6, 3), (5, 1), (7, 7)])
+def test_topk_brute_force(E, k):
+    rng = np.random.default_rng(E * 100 + k)
+    z = rng.normal(size=(40, E))
+    # forced ties: quantised logits and all-equal rows
+    zq = np.round(rng.normal(size=(40, E)) * 2) / 2
+    zeq = np.zeros((3, E))
+    for arr in (z, zq, zeq):
+        idx = O.topk_experts(arr, k)
+        for t in range(arr.shape[0]):
+            assert idx[t].tolist() == _brute_topk(arr[t], k)
+
+
+def test_topk_ties_go_to_lower_index():
+    z = np.array([[1.0, 3.0, 3.0, 1.0, 3.0]])
+    assert O.topk_experts(z, 2)[0].tolist() == [1, 2]
+    assert O.topk_experts(z, 4)[0].tolist() == [1, 2, 4, 0]
+
+
+# ---------------------------------------------------------------------------
+# Capacity and dispatch ("负载不均：路由坍缩与丢 token")
+# ---------------------------------------------------------------------------
+
+def test_capacity_worked_example(golden):
+    g = golden("moe10_capacity_example.json")
+    idx = np.array(g["choice"]).reshape(g["T"], g["k"])
+    for case in g["cases"]:
+        C = O.expert_capacity(g["T"], g["E"], case["capacity_factor"])
+        assert C == case["capacity"]
+        r = O.dispatch(idx, g["E"], C)
+        dropped = [t for t in range(g["T"]) if r["drop_mask"][t]]
+        assert dropped == case["dropped_tokens"]
+        assert int(r["drops"].sum()) == case["n_dropped"]
+
+
+def test_capacity_formula_values():
+    assert O.expert_capacity(8, 4, 1.25) == 3          # 2 x 1.25 = 2.5 -> 3
+    assert O.expert_capacity(16384, 64, 1.25) == 320   # Switch-shaped layer
+    assert O.expert_capacity(8, 4, None) is None
+
+
+def _check_dispatch_invariants(idx, E, C, r):
+    T, k = idx.shape
+    A = T * k
+    counts, drops, offsets, perm = r["counts"], r["drops"], r["offsets"], r["perm"]
+    assert counts.sum() + drops.sum() == A
+    if C is not None:
+        assert np.all(counts <= C)
+        # an expert drops only when full
+        assert np.all((drops == 0) | (counts == C))
+    assert offsets[0] == 0 and np.all(np.diff(offsets) == counts)
+    n = offsets[E]
+    kept = sorted(int(a) for a in perm[:n])
+    assert kept == [a for a in range(A) if r["drop_mask"][a] == 0]
+    flat = idx.reshape(A)
+    for e in range(E):
+        seg = perm[offsets[e]:offsets[e + 1]]
+        assert np.all(flat[seg] == e)
+        assert np.all(np.diff(seg) > 0)       # ascending assignment id
+    for a in range(A):
+        if r["drop_mask"][a]:
+            assert r["row_of"][a] == -1
+        else:
+            assert perm[r["row_of"][a]] == a
+    # fill order: every dropped assignment comes after all kept ones of its expert
+    for e in range(E):
+        ids = [a for a in range(A) if flat[a] == e]
+        dm = [r["drop_mask"][a] for a in ids]
+        assert dm == sorted(dm)
+
+
+@pytest.mark.parametrize("cf", [None, 0.5, 1.0, 1.25, 3.0])
+def test_dispatch_invariants_random(cf):
+    rng = np.random.default_rng(7)
+    T, E, k = 53, 6, 2
+    z = rng.normal(size=(T, E)) + np.linspace(1.5, 0, E)   # skewed load
+    idx = O.topk_experts(z, k)
+    C = O.expert_capacity(T, E, cf)
+    r = O.dispatch(idx, E, C)
+    _check_dispatch_invariants(idx, E, C, r)
+
+
+def test_dispatch_capacity_zero_and_large():
+    idx = np.array([[0, 1], [1, 0], [0, 2]])
+    r0 = O.dispatch(idx, 3, 0)
+    assert r0["counts"].tolist() == [0, 0, 0] and r0["drops"].tolist() == [3, 2, 1]
+    r9 = O.dispatch(idx, 3, 99)
+    assert r9["drops"].sum() == 0
+    assert r9["perm"][:6].tolist() == [0, 3, 4, 1, 2, 5]
+
+
+# ---------------------------------------------------------------------------
+# Balance term ("辅助损失") and parameter accounting ("总参数和激活参数怎样算")
+# ---------------------------------------------------------------------------
+
+def test_aux_loss_worked_values(golden):
+    for c in golden("moe10_aux_loss_example.json")["cases"]:
+        assert abs(O.switch_balance_term(c["f"], c["P"]) - c["value"]) < 1e-12
+
+
+def test_load_fractions_from_counts():
+    f = O.load_fractions(np.array([3, 1, 1, 1]), np.array([2, 0, 0, 0]))
+    np.testing.assert_allclose(f, [5 / 8, 1 / 8, 1 / 8, 1 / 8], rtol=1e-15)
+
+
+def test_mixtral_param_closed_form(golden):
+    m = golden("moe10_param_counts.json")["mixtral_8x7b"]
+    d, E, k, F = m["d"], m["E"], m["k"], m["F"]
+    assert O.moe_layer_params(d, 1, F) - d == m["per_expert"]
+    assert O.moe_layer_params(d, E, 0) == m["router_per_layer"]
+    rest = m["attention_per_layer"] + m["norms_per_layer"]
+    total = m["layers"] * (rest + O.moe_layer_params(d, E, F)) + m["embed_and_head"] + m["final_norm"]
+    active = m["layers"] * (rest + O.moe_layer_params(d, E, F, k=k)) + m["embed_and_head"] + m["final_norm"]
+    assert total == m["total"]
+    assert active == m["active"]
+
+
+def test_deepseek_v3_param_closed_form(golden):
+    m = golden("moe10_param_counts.json")["deepseek_v3"]
+    d, E, k, F, Fs, L = m["d"], m["E"], m["k"], m["F"], m["F_s"], m["moe_layers"]
+    assert O.moe_layer_params(d, 1, F) - d == m["per_expert"]
+    fixed = m["mla_all_layers"] + m["dense_ffn_first_3"] + m["embed_and_head"] + m["norms"]
+    assert fixed + L * O.moe_layer_params(d, E, F, Fs) == m["total"]
+    assert fixed + L * O.moe_layer_params(d, E, F, Fs, k=k) == m["active"]
+
+
+def test_decode_expert_usage(golden):
+    u = golden("moe10_param_counts.json")["decode_usage"]
+    for B, pct in u["batch_to_percent"].items():
+        frac = O.expected_touched_experts(u["E"], u["k"], int(B)) / u["E"]
+        assert round(100 * frac) == pct
+
+
+# ---------------------------------------------------------------------------
+# Expert FFN closed forms
+# ---------------------------------------------------------------------------
+
+def test_silu_closed_values():
+    # SiLU(u) = u sigma(u); sigma(ln 3) = 3/4 exactly
+    u = np.array([math.log(3.0), -math.log(3.0), 0.0])
+    np.testing.assert_allclose(O.silu(u), [0.75 * math.log(3.0), -0.25 * math.log(3.0), 0.0],
+                               rtol=1e-15, atol=1e-300)
+
+
+def test_swiglu_permutation_experts():
+    # One-hot weights make every projection a coordinate pick, so the FFN is a
+    # closed form that changes if any operand is transposed:
+    #   gate_f = x[pg[f]], up_f = x[pu[f]], y_i = h[pd[i]]
+    d, F = 3, 4
+    pg, pu, pd = [2, 0, 1, 2], [1, 1, 0, 2], [3, 0, 2]
+    Wg = np.zeros((F, d)); Wu = np.zeros((F, d)); Wd = np.zeros((d, F))
+    for f in range(F):
+        Wg[f, pg[f]] = 1.0
+        Wu[f, pu[f]] = 1.0
+    for i in range(d):
+        Wd[i, pd[i]] = 1.0
+    x = np.array([[math.log(3.0), 2.0, -math.log(3.0)]])
+    sil = {0: 0.75 * math.log(3.0), 2: -0.25 * math.log(3.0)}   # SiLU(x[c]) for c=0,2
+    sil[1] = 2.0 / (1.0 + math.exp(-2.0))
+    h = [sil[pg[f]] * x[0, pu[f]] for f in range(F)]
+    want = [h[pd[i]] for i in range(d)]
+    np.testing.assert_allclose(O.swiglu_ffn(x, Wg, Wu, Wd)[0], want, rtol=1e-14)
+
+
+def test_router_logits_hand_example():
+    x = np.array([[1.0, 2.0]])
+    W = np.array([[1.0, 0.0], [0.0, 1.0], [1.0, 1.0]])   # [E=3, d=2]
+    assert O.router_logits(x, W)[0].tolist() == [1.0, 2.0, 3.0]
+    assert O.router_logits(x, W, np.array([0.5, 0.0, -1.0]))[0].tolist() == [1.5, 2.0, 2.0]
+
+
+# ---------------------------------------------------------------------------
+# Layer special cases
+# ---------------------------------------------------------------------------
+
+def _rand_layer(rng, T, d, E, F, Fs=0):
+    x = rng.normal(size=(T, d))
+    wr = rng.normal(size=(E, d)) / math.sqrt(d)
+    ex = [(rng.normal(size=(F, d)) / math.sqrt(d), rng.normal(size=(F, d)) / math.sqrt(d),
+           rng.normal(size=(d, F)) / math.sqrt(F)) for _ in range(E)]
+    sh = None
+    if Fs:
+        sh = (rng.normal(size=(Fs, d)) / math.sqrt(d), rng.normal(size=(Fs, d)) / math.sqrt(d),
+              rng.normal(size=(d, Fs)) / math.sqrt(Fs))
+    return x, wr, ex, sh
+
+
+def test_single_expert_is_dense_swiglu():
+    rng = np.random.default_rng(3)
+    x, wr, ex, _ = _rand_layer(rng, 9, 5, 1, 7)
+    r = O.moe_layer_forward(x, wr, ex, k=1, gate="softmax", renormalize=True)
+    np.testing.assert_allclose(r["y"], O.swiglu_ffn(x, *ex[0]), rtol=1e-13, atol=1e-14)
+
+
+@pytest.mark.parametrize("gate,rsf", [("softmax", 1.0), ("sigmoid", 2.5)])
+def test_identical_experts_sum_of_weights(gate, rsf):
+    rng = np.random.default_rng(4)
+    x, wr, ex, sh = _rand_layer(rng, 11, 6, 5, 8, Fs=4)
+    same = [ex[0]] * 5
+    r = O.moe_layer_forward(x, wr, same, k=3, gate=gate, renormalize=True,
+                            routed_scaling_factor=rsf, shared=sh)
+    want = rsf * O.swiglu_ffn(x, *ex[0]) + O.swiglu_ffn(x, *sh)
+    np.testing.assert_allclose(r["y"], want, rtol=1e-12, atol=1e-13)
+
+
+def test_k_equals_E_is_full_softmax_mixture():
+    rng = np.random.default_rng(5)
+    x, wr, ex, _ = _rand_layer(rng, 7, 4, 3, 6)
+    r = O.moe_layer_forward(x, wr, ex, k=3, gate="softmax", renormalize=True)
+    z = x @ wr.T
+    p = np.exp(z) / np.exp(z).sum(axis=1, keepdims=True)
+    want = sum(p[:, [e]] * O.swiglu_ffn(x, *ex[e]) for e in range(3))
+    np.testing.assert_allclose(r["y"], want, rtol=1e-12, atol=1e-13)
+
+
+def test_capacity_zero_leaves_shared_only():
+    rng = np.random.default_rng(6)
+    x, wr, ex, sh = _rand_layer(rng, 6, 4, 3, 5, Fs=3)
+    r = O.moe_layer_forward(x, wr, ex, k=2, gate="softmax", renormalize=True,
+                            capacity=0, shared=sh)
+    np.testing.assert_allclose(r["y"], O.swiglu_ffn(x, *sh), rtol=1e-14)
+    r2 = O.moe_layer_forward(x, wr, ex, k=2, gate="softmax", renormalize=True, capacity=0)
+    assert np.all(r2["y"] == 0.0)
+
+
+@pytest.mark.parametrize("cap,gate,renorm,rsf", [(None, "softmax", True, 1.0),
+                                                 (3, "softmax", False, 1.0),
+                                                 (4, "sigmoid", True, 2.5)])
+def test_two_formulations_agree(cap, gate, renorm, rsf):
+    rng = np.random.default_rng(8)
+    x, wr, ex, sh = _rand_layer(rng, 17, 6, 5, 7, Fs=5)
+    bias = -1.2 * np.log(np.arange(5) + 1.0)
+    r = O.moe_layer_forward(x, wr, ex, k=2, gate=gate, renormalize=renorm,
+                            routed_scaling_factor=rsf, capacity=cap,
+                            router_bias=bias, shared=sh)
+    y2 = O.moe_layer_forward_token_loop(x, wr, ex, k=2, gate=gate, renormalize=renorm,
+                                        routed_scaling_factor=rsf, capacity=cap,
+                                        router_bias=bias, shared=sh)
+    np.testing.assert_allclose(r["y"], y2, rtol=1e-12, atol=1e-13)
+
+
+def test_token_subset_matches_full():
+    rng = np.random.default_rng(9)
+    x, wr, ex, sh = _rand_layer(rng, 20, 4, 4, 6, Fs=2)
+    full = O.moe_layer_forward(x, wr, ex, k=2, gate="softmax", renormalize=True,
+                               capacity=6, shared=sh)
+    sub = O.moe_layer_forward(x, wr, ex, k=2, gate="softmax", renormalize=True,
+                              capacity=6, shared=sh, tokens=[19, 3, 11])
+    np.testing.assert_allclose(sub["y"], full["y"][[19, 3, 11]], rtol=1e-14)
+
+
+def test_dropped_assignment_contributes_zero_no_rerenorm():
+    # token 2's first choice is dropped at capacity 2; its second choice keeps
+    # its original weight (no second renormalisation).
+    d, F, E = 2, 3, 3
+    x = np.array([[1.0, 0.0], [1.0, 0.1], [1.0, -0.2]])
+    wr = np.array([[2.0, 0.0], [0.0, 1.0], [0.0, -1.0]])
+    rng = np.random.default_rng(10)
+    ex = [(rng.normal(size=(F, d)), rng.normal(size=(F, d)), rng.normal(size=(d, F)))
+          for _ in range(E)]
+    r = O.moe_layer_forward(x, wr, ex, k=2, gate="softmax", renormalize=True, capacity=2)
+    assert r["topk_idx"][:, 0].tolist() == [0, 0, 0]
+    assert r["drop_mask"].reshape(3, 2)[2].tolist() == [1, 0]
+    g = r["topk_w"]
+    assert r["topk_idx"][2].tolist() == [0, 2]
+    want = g[2, 1] * O.swiglu_ffn(x[2:3], *ex[2])[0]
+    np.testing.assert_allclose(r["y"][2], want, rtol=1e-14)

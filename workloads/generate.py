@@ -1,0 +1,114 @@
+"""Seeded synthetic tensors for an MoE layer shape.
+
+Recipe (one torch.Generator stream per tensor, seeded from the tensor's name):
+
+* x        ~ N(0, 1)          [T, d]
+* w_router ~ N(0, 1/d)        [E, d]      (nn.Linear orientation: out x in)
+* w_gate   ~ N(0, 1/d)        [E, F, d]   one stream per expert
+* w_up     ~ N(0, 1/d)        [E, F, d]
+* w_down   ~ N(0, 1/F)        [E, d, F]
+* ws_gate, ws_up ~ N(0, 1/d)  [F_s, d]    shared expert (when F_s > 0)
+* ws_down  ~ N(0, 1/F_s)      [d, F_s]
+* router_bias (Zipf-skewed shapes only): b_e = -s * ln(e + 1), the log of an
+  unnormalised Zipf(s) mass, so expert 0 is the hottest.  The normaliser of
+  the Zipf pmf would cancel under softmax and under the argmax, so it is left
+  out.
+
+Values are drawn in float32 and then cast to the shape's dtype (bf16 or fp32).
+This module holds no routing or expert arithmetic.
+"""
+
+from __future__ import annotations
+
+import math
+import zlib
+from dataclasses import dataclass
+from typing import Dict, Optional
+
+import numpy as np
+import torch
+
+from .shapes import MoEShape
+
+_DTYPES = {"bf16": torch.bfloat16, "fp32": torch.float32}
+
+
+def tensor_seed(seed_base: int, name: str) -> int:
+    """Deterministic per-tensor seed: CRC32 of "<seed_base>:<name>"."""
+    return zlib.crc32(f"{seed_base}:{name}".encode()) & 0x7FFFFFFF
+
+
+def _normal(shape, std: float, name: str, seed_base: int, device, dtype) -> torch.Tensor:
+    g = torch.Generator(device=device)
+    g.manual_seed(tensor_seed(seed_base, name))
+    t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(dtype)
+
+
+def make_inputs(shape: MoEShape, device="cpu", seed: int = 0,
+                with_experts: bool = True) -> Dict[str, Optional[torch.Tensor]]:
+    """All tensors of one layer instance, on ``device``.
+
+    Returns a dict with keys x, w_router, router_bias, w_gate, w_up, w_down,
+    ws_gate, ws_up, ws_down (absent parts are None).
+    """
+    dt = _DTYPES[shape.dtype]
+    T, d, E, F, Fs = shape.T, shape.d, shape.E, shape.F, shape.F_s
+    out: Dict[str, Optional[torch.Tensor]] = {}
+    out["x"] = _normal((T, d), 1.0, "x", seed, device, dt)
+    out["w_router"] = _normal((E, d), 1.0 / math.sqrt(d), "w_router", seed, device, dt)
+    if shape.zipf_s is not None:
+        e = torch.arange(E, dtype=torch.float64)
+        out["router_bias"] = (-shape.zipf_s * torch.log(e + 1.0)).to(torch.float32).to(device)
+    else:
+        out["router_bias"] = None
+    if with_experts:
+        wg = torch.empty((E, F, d), dtype=dt, device=device)
+        wu = torch.empty((E, F, d), dtype=dt, device=device)
+        wd = torch.empty((E, d, F), dtype=dt, device=device)
+        for e in range(E):
+            wg[e] = _normal((F, d), 1.0 / math.sqrt(d), f"w_gate.{e}", seed, device, dt)
+            wu[e] = _normal((F, d), 1.0 / math.sqrt(d), f"w_up.{e}", seed, device, dt)
+            wd[e] = _normal((d, F), 1.0 / math.sqrt(F), f"w_down.{e}", seed, device, dt)
+        out["w_gate"], out["w_up"], out["w_down"] = wg, wu, wd
+        if Fs > 0:
+            out["ws_gate"] = _normal((Fs, d), 1.0 / math.sqrt(d), "ws_gate", seed, device, dt)
+            out["ws_up"] = _normal((Fs, d), 1.0 / math.sqrt(d), "ws_up", seed, device, dt)
+            out["ws_down"] = _normal((d, Fs), 1.0 / math.sqrt(Fs), "ws_down", seed, device, dt)
+        else:
+            out["ws_gate"] = out["ws_up"] = out["ws_down"] = None
+    return out
+
+
+def to_f64(t: Optional[torch.Tensor]) -> Optional[np.ndarray]:
+    """Exact widening of a bf16/fp32 tensor (any device) to a float64 array."""
+    if t is None:
+        return None
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+@dataclass
+class ExpertWeights:
+    """Lazy per-expert float64 view of the expert weight tensors.
+
+    ``weights[e]`` returns (w_gate_e [F,d], w_up_e [F,d], w_down_e [d,F]) as
+    float64 arrays, converting one expert at a time so that a 22 GB bf16 layer
+    never has to exist as a 90 GB float64 copy.
+    """
+    w_gate: torch.Tensor
+    w_up: torch.Tensor
+    w_down: torch.Tensor
+
+    def __len__(self) -> int:
+        return self.w_gate.shape[0]
+
+    def __getitem__(self, e: int):
+        return to_f64(self.w_gate[e]), to_f64(self.w_up[e]), to_f64(self.w_down[e])
+
+
+def shared_weights(inputs) -> Optional[tuple]:
+    if inputs.get("ws_gate") is None:
+        return None
+    return to_f64(inputs["ws_gate"]), to_f64(inputs["ws_up"]), to_f64(inputs["ws_down"])
