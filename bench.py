@@ -1,0 +1,437 @@
+#!/usr/bin/env python
+"""MoE layer forward throughput on B300 (one JSON line on rank 0).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one full moe_layer_forward (router, gating/top-k, capacity/dispatch,
+gather, grouped gate/up + SwiGLU, grouped down, combine) over one batch of
+synthetic inputs that are already resident in HBM.  ``value`` is tokens/s over
+all ranks; with N > 1 every rank runs an independent replica (the layer shards
+by tokens with no exchange), so scaling is weak.
+
+--impl reference times the float64 CPU oracle (the only reference
+implementation: the pages print no code) on the host cores, on a bounded
+sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("MoE-layer tokens/s on 1 B300; % of bf16 tensor peak (prefill) / "
+          "HBM BW (decode)")
+
+WORKLOAD_TEXT = {
+    "mixtral": "Mixtral-8x7B-shaped MoE layer (T=4096, d=4096, E=8, top-2, SwiGLU d_ff=14336, "
+               "softmax + renorm, bf16, fp32 accumulate)",
+    "dsv3_prefill": "DeepSeek-V3-shaped MoE prefill layer (T=8192, d=7168, E=256 top-8, "
+                    "d_ff=2048, 1 shared expert d_ff=2048, sigmoid, renorm x2.5, bf16)",
+    "switch": "Switch-style capacity layer (T=16384, d=2048, E=64 top-1, d_ff=8192, softmax, "
+              "C=ceil(T/E*1.25)=320, Zipf(1.2) router bias, bf16)",
+    "dsv3_decode": "DeepSeek-V3-shaped decode layer (T=64, d=7168, E=256 top-8, d_ff=2048, "
+                   "1 shared expert, sigmoid, renorm x2.5, bf16)",
+    "tiny": "tiny fp32 layer (T=64, d=128, E=4 top-2, d_ff=256)",
+}
+
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mixtral", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample-tokens", type=int, default=16)
+    ap.add_argument("--cpu-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# environment helpers
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest() -> str:
+    """Digest of the CUDA sources, to tell whether stored ncu counters still
+    describe the current kernels."""
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "top_routing_expert_gate_b300", "csrc", "*")))
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload: str, stage: str):
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    rec = t.get(workload, {}).get(stage)
+    if not rec or rec.get("source_digest") != source_digest():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        self.dev = device_index
+
+    def _smi_id(self):
+        import torch
+        try:
+            p = torch.cuda.get_device_properties(self.dev)
+            return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            return vis.split(",")[self.dev] if vis else str(self.dev)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", self._smi_id()],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work
+# ---------------------------------------------------------------------------
+
+def algorithmic_work(shape, counts):
+    """FLOPs and bytes of one forward: router + kept assignments + shared."""
+    T, d, E, F, Fs = shape.T, shape.d, shape.E, shape.F, shape.F_s
+    kept = int(sum(counts))
+    touched = int(sum(1 for c in counts if c > 0))
+    eb = 2 if shape.dtype == "bf16" else 4
+    fl_router = 2.0 * T * E * d
+    fl_gate_up = 2.0 * kept * 2 * F * d + 2.0 * T * 2 * Fs * d
+    fl_down = 2.0 * kept * F * d + 2.0 * T * Fs * d
+    w_bytes_touched = touched * 3 * d * F * eb + 3 * d * Fs * eb + E * d * eb
+    return {"kept": kept, "touched": touched, "flops_router": fl_router,
+            "flops_gate_up": fl_gate_up, "flops_down": fl_down,
+            "flops": fl_router + fl_gate_up + fl_down,
+            "bytes_gate_up": touched * 2 * d * F * eb + 2 * d * Fs * eb,
+            "bytes_down": touched * d * F * eb + d * Fs * eb,
+            "weight_bytes": w_bytes_touched}
+
+
+# ---------------------------------------------------------------------------
+# float64 oracle timing (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+def time_oracle(shape, inputs, sample_tokens: int, steps: int, warmup: int = 0):
+    """Oracle forward on the host: routing of all T tokens and the layer output
+    of ``sample_tokens`` tokens per step.  Expert weights are widened to f64 once
+    before timing (resident, as the GPU's weights are resident in HBM)."""
+    import numpy as np
+    from oracle import moe_oracle as O
+    from workloads.generate import to_f64
+
+    x = to_f64(inputs["x"])
+    wr = to_f64(inputs["w_router"])
+    bias = to_f64(inputs["router_bias"])
+    E = shape.E
+    experts = [(to_f64(inputs["w_gate"][e]), to_f64(inputs["w_up"][e]),
+                to_f64(inputs["w_down"][e])) for e in range(E)]
+    shared = None
+    if inputs.get("ws_gate") is not None:
+        shared = (to_f64(inputs["ws_gate"]), to_f64(inputs["ws_up"]), to_f64(inputs["ws_down"]))
+    cap = O.expert_capacity(shape.T, shape.E, shape.capacity_factor)
+    rng = np.random.default_rng(0)
+    times = []
+    for i in range(warmup + steps):
+        toks = np.sort(rng.choice(shape.T, size=min(sample_tokens, shape.T), replace=False))
+        t0 = time.perf_counter()
+        O.moe_layer_forward(x, wr, experts, k=shape.k, gate=shape.gate,
+                            renormalize=shape.renormalize, routed_scaling_factor=shape.rsf,
+                            capacity=cap, router_bias=bias, shared=shared, tokens=toks)
+        if i >= warmup:
+            times.append(time.perf_counter() - t0)
+    return times
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def main(argv=None):
+    args = parse_args(argv)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    import torch
+    import torch.distributed as dist
+
+    from workloads import SHAPES, make_inputs
+
+    shape = SHAPES[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local_rank)
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        inputs = make_inputs(shape, device=dev, seed=0)
+        times = time_oracle(shape, inputs, args.cpu_sample_tokens, args.steps, args.warmup)
+        t = statistics.mean(times)
+        val = args.cpu_sample_tokens / t
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * t, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
+                "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores_used(),
+                                 "kind": "oracle",
+                                 "sample": f"per step: routing of all {shape.T} tokens + layer "
+                                           f"output of {args.cpu_sample_tokens} sampled tokens"},
+                "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import top_routing_expert_gate_b300 as moe
+    from top_routing_expert_gate_b300 import _binding as B
+
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    inputs = make_inputs(shape, device=dev, seed=0)
+    cfg = moe.config_from_shape(shape, out_dtype="fp32")
+    ws = moe.Workspace(cfg, dev)
+    w = moe.LayerWeights.from_inputs(inputs)
+    T, d, E, k = shape.T, shape.d, shape.E, shape.k
+    x = inputs["x"]
+    y = torch.empty((T, d), dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    drops = torch.empty(E, dtype=torch.int32, device=dev)
+    mean_prob = torch.empty(E, dtype=torch.float32, device=dev)
+    topk_idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    NS = B.MOE_NUM_STAGES
+
+    def new_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)      # creates the underlying cudaEvent
+        return evs
+
+    step_events = [new_events(NS + 1) for _ in range(args.steps)]
+    warm_events = new_events(NS + 1)
+
+    def step(evs):
+        return moe.moe_layer_forward_profiled(cfg, x, w.w_router, w.router_bias, w.w_gate,
+                                              w.w_up, w.w_down, w.ws_gate, w.ws_up, w.ws_down,
+                                              y, topk_idx, topk_w, counts, drops, mean_prob,
+                                              ws, evs, stream)
+
+    for _ in range(args.warmup):
+        step(warm_events)
+    torch.cuda.synchronize(dev)
+    status = moe.moe_get_error(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+    counts_host = counts.cpu().tolist()
+    work = algorithmic_work(shape, counts_host)
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    launches = 0
+    t_start.record(stream)
+    for i in range(args.steps):
+        launches += step(step_events[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = tt.item()
+    ms_per_step = total_ms / args.steps
+    status = moe.moe_get_error(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed steps")
+
+    stage_ms = {}
+    for si, name in enumerate(B.STAGE_NAMES):
+        vals = [ev[si].elapsed_time(ev[si + 1]) for ev in step_events]
+        stage_ms[name] = sum(vals) / len(vals)
+
+    # end to end through the public API: pinned host x in, y out, every step
+    x_host = x.cpu().pin_memory()
+    y_host = torch.empty((T, d), dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(x)
+    e2e_start = torch.cuda.Event(enable_timing=True)
+    e2e_end = torch.cuda.Event(enable_timing=True)
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.layer_forward(cfg, x_dev, w, ws=ws, y=y, stats=False)
+        y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e2e_start.record(stream)
+    for _ in range(args.e2e_steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.layer_forward(cfg, x_dev, w, ws=ws, y=y, stats=False)
+        y_host.copy_(y, non_blocking=True)
+    e2e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e2e_start.elapsed_time(e2e_end) / args.e2e_steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = tt.item()
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    # dominant stage: the longest one
+    dom = max(stage_ms, key=stage_ms.get)
+    if dom in ("gate_up", "down") and shape.T >= 1024:
+        flops = work["flops_gate_up"] if dom == "gate_up" else work["flops_down"]
+        achieved = flops / (stage_ms[dom] * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "kernel": f"grouped_{dom}", "achieved": achieved,
+                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"bf16_tflops ({peak_src})"}
+    else:
+        nbytes = work["bytes_gate_up"] if dom == "gate_up" else (
+            work["bytes_down"] if dom == "down" else work["weight_bytes"])
+        achieved = nbytes / (stage_ms[dom] * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "kernel": f"grouped_{dom}" if dom in ("gate_up", "down") else dom,
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"hbm_gbs ({peak_src})"}
+    roof["traffic"] = stored_traffic(args.workload, dom)
+
+    value = world * T / (ms_per_step * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": shape.dtype,
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
+                   "global_batch_tokens": world * T, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: every step streams "
+                         f"{work['weight_bytes'] / 1e9:.2f} GB of expert weights (L2 126 MB)",
+                   "kept_assignments": work["kept"], "touched_experts": work["touched"]},
+        "tflops": work["flops"] / (ms_per_step * 1e-3) / 1e12,
+        "tensor_peak_frac": work["flops"] / (ms_per_step * 1e-3) / 1e12 / peaks["bf16_tflops"],
+        "weight_gbs": work["weight_bytes"] / (ms_per_step * 1e-3) / 1e9,
+        "stage_ms": stage_ms,
+        "roofline": roof,
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x.numel() * x.element_size(),
+                "d2h_bytes_per_step": y.numel() * y.element_size()},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        times = time_oracle(shape, inputs, args.cpu_sample_tokens, args.cpu_steps)
+        t = statistics.mean(times)
+        line["cpu_baseline"] = {"value": args.cpu_sample_tokens / t, "unit": "tokens/s",
+                                "cores": cores_used(), "kind": "oracle",
+                                "sample": f"{args.cpu_steps} oracle steps, each: routing of all "
+                                          f"{T} tokens + layer output of "
+                                          f"{args.cpu_sample_tokens} sampled tokens"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,224 @@
+/*
+ * moe_b300.h - C ABI of the single-GPU MoE FFN layer forward (NVIDIA B300,
+ * sm_103a).
+ *
+ * The layer, as the pages state it:
+ *   logits = x . W_router^T                     ("10. 混合专家 MoE：总参数与激活参数",
+ *                                                 niuwancheng.cn, block sketch in
+ *                                                 "把一个大 FFN 换成一组小 FFN")
+ *   score  = softmax(logits) or sigmoid(logits) (same page, "路由器怎样选专家：
+ *                                                 top-k 与两种门控")
+ *   top-k on the logits; weights renormalised over the chosen k and times
+ *   routed_scaling_factor (same section)
+ *   capacity = ceil((T / E) * capacity_factor); over-capacity assignments are
+ *   dropped and ride the residual (same page, "负载不均：路由坍缩与丢 token")
+ *   y_t = sum_{i in TopK} g_{t,i} E_i(x_t) + S(x_t)   ("MoE为什么只激活一部分专家",
+ *                                                 hi-bin.com, "Router 怎样给 Token
+ *                                                 选专家"; shared expert S from
+ *                                                 "细粒度专家与共享专家")
+ *   E_i(x) = (SiLU(x W_gate,i^T) * (x W_up,i^T)) W_down,i^T
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates device memory: each call takes a workspace `ws` of at
+ *     least moe_workspace_size() bytes, 256-byte aligned, zero-filled once
+ *     before its first use (moe_workspace_init does this).  One workspace must
+ *     not be used by two calls that may run concurrently.
+ *   - Every compute call is asynchronous on the caller's `stream` (a
+ *     cudaStream_t passed as void*, NULL = the legacy default stream).  No call
+ *     synchronises the stream or copies device data to the host, except
+ *     moe_get_error.
+ *   - Argument errors are detected on the host before anything is enqueued and
+ *     returned synchronously; nothing is launched then.  Launch errors return
+ *     MOE_ERR_CUDA.  Errors found by kernels (a bounded wait that ran out, an
+ *     index out of range) are recorded in a status word inside `ws` and
+ *     reported by moe_get_error.
+ *   - Layouts are row-major with nn.Linear orientation (out x in):
+ *       x [T, d], w_router [E, d], w_gate / w_up [E, F, d], w_down [E, d, F],
+ *       ws_gate / ws_up [F_s, d], ws_down [d, F_s].
+ *     Activations and weights have dtype act_dtype (MOE_BF16 or MOE_FP32);
+ *     accumulation is always fp32.  Logits, weights and statistics are fp32.
+ *   - Assignment a = t * top_k + j is token t's j-th choice (j = 0 best).
+ *   - Pointers must be 16-byte aligned.  For MOE_BF16, d_model must be a
+ *     multiple of 64 and d_ff / d_ff_shared multiples of 128 (the tensor-core
+ *     tiles); otherwise MOE_ERR_UNSUPPORTED.  1 <= top_k <= n_experts <= 256.
+ *   - No C++ exception crosses this boundary.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment, k > E  */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid but outside what the kernels implement */
+  MOE_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed            */
+  MOE_ERR_WORKSPACE = 4,    /* workspace null or too small                  */
+  MOE_ERR_TIMEOUT = 5,      /* a kernel's bounded wait ran out (moe_get_error) */
+  MOE_ERR_DEVICE = 6        /* a kernel found an inconsistent index (moe_get_error) */
+} moe_status_t;
+
+typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID = 1 } moe_gate_t;
+typedef enum { MOE_BF16 = 0, MOE_FP32 = 1 } moe_dtype_t;
+
+/* Layer description.  All fields are plain 32-bit values. */
+typedef struct {
+  int32_t T;              /* tokens in the batch, >= 0                          */
+  int32_t d_model;        /* d                                                  */
+  int32_t n_experts;      /* E, routed experts, 1..256                          */
+  int32_t top_k;          /* k, 1..E                                            */
+  int32_t d_ff;           /* F, routed expert SwiGLU width                      */
+  int32_t d_ff_shared;    /* F_s, shared expert width; 0 = no shared expert     */
+  int32_t gate;           /* moe_gate_t                                         */
+  int32_t renormalize;    /* 1: g_j = score_j / sum_chosen score; 0: g_j = score_j */
+  float routed_scaling_factor; /* multiplies every routed weight (1.0, or 2.5)  */
+  int32_t capacity;       /* < 0: unlimited; >= 0: kept slots per expert (0 drops all) */
+  int32_t act_dtype;      /* moe_dtype_t of x, weights and the expert activations */
+  int32_t out_dtype;      /* moe_dtype_t of y                                   */
+} moe_config_t;
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+MOE_API int32_t moe_version(void);
+
+/* Human-readable name of a status code (static storage). */
+MOE_API const char* moe_status_string(moe_status_t st);
+
+/* Expert capacity ceil((T / E) * capacity_factor), computed in IEEE double in
+ * that order ("负载不均：路由坍缩与丢 token": 2 x 1.25 = 2.5 is rounded up to 3).
+ * Returns -1 for T < 0, E <= 0 or capacity_factor < 0 (or NaN). */
+MOE_API int32_t moe_capacity(int32_t T, int32_t E, double capacity_factor);
+
+/* Bytes of workspace every call below needs for this configuration. */
+MOE_API moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
+
+/* Clears the workspace's device status word (cudaMemsetAsync on `stream`).
+ * Call once after allocating the workspace. */
+MOE_API moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_bytes,
+                                void* stream);
+
+/* Router + gating + top-k (the block sketch's first four lines).
+ *   x [T, d] act_dtype; w_router [E, d] act_dtype;
+ *   router_bias [E] fp32 or NULL: added to every logit before scoring and
+ *     selection (used by the Zipf-skewed Switch-style layer);
+ *   logits_out [T, E] fp32 or NULL: the logits incl. bias;
+ *   topk_idx [T, k] int32: chosen experts, logit descending, ties to the
+ *     lower expert index;
+ *   topk_w [T, k] fp32: combine weights (renormalised and scaled per cfg);
+ *   mean_prob [E] fp32 or NULL: (1/T) sum_t score[t, e] over ALL experts
+ *     (softmax probability or sigmoid score), reduced in a fixed order. */
+MOE_API moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x, const void* w_router,
+                             const float* router_bias, float* logits_out,
+                             int32_t* topk_idx, float* topk_w, float* mean_prob,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* Gating + top-k from caller-supplied fp32 logits [T, E] (bias already in).
+ * Outputs as moe_router_topk.  The selection compares fp32 logits only, so
+ * it is reproducible bit for bit from the same logits. */
+MOE_API moe_status_t moe_topk_from_logits(const moe_config_t* cfg, const float* logits,
+                                  int32_t* topk_idx, float* topk_w, float* mean_prob,
+                                  void* ws, size_t ws_bytes, void* stream);
+
+/* Capacity + dispatch ("负载不均：路由坍缩与丢 token"; the block sketch's
+ * per-expert grouping).  Assignments are visited in ascending a; each takes
+ * the next free slot of its expert or is dropped once the expert holds
+ * cfg->capacity.  Deterministic (no order-dependent atomics).
+ *   topk_idx [T, k] int32 (values in [0, E); others -> MOE_ERR_DEVICE);
+ *   counts [E] int32: kept assignments per expert;
+ *   drops [E] int32: dropped assignments per expert;
+ *   offsets [E + 1] int32: exclusive prefix sum of counts;
+ *   perm [T * k] int32: perm[offsets[e] + slot] = a; entries at and beyond
+ *     offsets[E] are left unspecified;
+ *   drop_mask [T * k] uint8: 1 where assignment a was dropped. */
+MOE_API moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* topk_idx,
+                          int32_t* counts, int32_t* drops, int32_t* offsets,
+                          int32_t* perm, uint8_t* drop_mask,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* Grouped SwiGLU experts over dispatched rows (the grouped GEMM that replaces
+ * the block sketch's per-expert loop).  Row r < offsets[E] of the grouped
+ * batch is token perm[r] / k and belongs to the expert whose segment holds r:
+ *   y_perm[r, :] = E_e(x[perm[r] / k, :])            fp32 [T * k, d]
+ * Rows at and beyond offsets[E] are left unspecified.  If the shared expert
+ * weights are given (cfg->d_ff_shared > 0), also
+ *   y_shared[t, :] = S(x[t, :])                      fp32 [T, d]
+ * ws_gate/ws_up/ws_down/y_shared must all be NULL when d_ff_shared == 0. */
+MOE_API moe_status_t moe_grouped_swiglu(const moe_config_t* cfg, const void* x,
+                                const int32_t* perm, const int32_t* offsets,
+                                const void* w_gate, const void* w_up, const void* w_down,
+                                const void* ws_gate, const void* ws_up, const void* ws_down,
+                                float* y_perm, float* y_shared,
+                                void* ws, size_t ws_bytes, void* stream);
+
+/* Weighted unpermute-combine:
+ *   y[t, :] = sum_{j: drop_mask[t*k+j] == 0} topk_w[t, j] * y_perm[row(t*k+j), :]
+ *             + y_shared[t, :]   (if y_shared != NULL)
+ * where row(a) is the r with perm[r] == a.  Summed in fp32 in ascending j,
+ * then the shared term; written once as out_dtype.  Tokens whose choices were
+ * all dropped get y_shared[t] or 0: y excludes the residual. */
+MOE_API moe_status_t moe_combine(const moe_config_t* cfg, const float* y_perm, const float* topk_w,
+                         const int32_t* offsets, const int32_t* perm,
+                         const uint8_t* drop_mask, const float* y_shared, void* y,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* The whole layer forward, stream-ordered, with no host synchronisation:
+ * router -> gating/top-k -> capacity/dispatch -> gather -> grouped gate/up +
+ * SwiGLU -> grouped down -> combine.
+ *   y [T, d] out_dtype (required);
+ *   router_bias, ws_gate/ws_up/ws_down (all or none) may be NULL;
+ *   topk_idx [T, k], topk_w [T, k], counts [E], drops [E], mean_prob [E]
+ *     are optional outputs (NULL = not returned). */
+MOE_API moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const void* w_router,
+                               const float* router_bias,
+                               const void* w_gate, const void* w_up, const void* w_down,
+                               const void* ws_gate, const void* ws_up, const void* ws_down,
+                               void* y, int32_t* topk_idx, float* topk_w,
+                               int32_t* counts, int32_t* drops, float* mean_prob,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/* Stages of moe_layer_forward, in launch order (for moe_layer_forward_profiled). */
+typedef enum {
+  MOE_STAGE_ROUTER = 0,    /* router logits                                  */
+  MOE_STAGE_TOPK = 1,      /* gating + top-k + mean probability              */
+  MOE_STAGE_DISPATCH = 2,  /* histogram, scan, scatter                       */
+  MOE_STAGE_GATHER = 3,    /* grouped rows of x                              */
+  MOE_STAGE_GATE_UP = 4,   /* grouped gate/up GEMM + SwiGLU                  */
+  MOE_STAGE_DOWN = 5,      /* grouped down GEMM                              */
+  MOE_STAGE_COMBINE = 6,   /* weighted unpermute-combine                     */
+  MOE_NUM_STAGES = 7
+} moe_stage_t;
+
+/* moe_layer_forward that also records stage_events[i] (cudaEvent_t, created
+ * by the caller) on `stream` right before stage i is enqueued, and
+ * stage_events[MOE_NUM_STAGES] after the last one, so that the caller can
+ * time each stage with cudaEventElapsedTime.  *n_launches (if not NULL)
+ * receives the number of kernels this call enqueued.  Same results as
+ * moe_layer_forward. */
+MOE_API moe_status_t moe_layer_forward_profiled(
+    const moe_config_t* cfg, const void* x, const void* w_router, const float* router_bias,
+    const void* w_gate, const void* w_up, const void* w_down, const void* ws_gate,
+    const void* ws_up, const void* ws_down, void* y, int32_t* topk_idx, float* topk_w,
+    int32_t* counts, int32_t* drops, float* mean_prob, void* ws, size_t ws_bytes, void* stream,
+    void** stage_events, int32_t* n_launches);
+
+/* Synchronises `stream`, reads and clears the workspace status word.
+ * Returns MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (or MOE_ERR_CUDA if the
+ * stream itself reports an error). */
+MOE_API moe_status_t moe_get_error(const void* ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

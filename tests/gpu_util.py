@@ -1,0 +1,75 @@
+"""Helpers shared by the GPU parity tests (comparison rules and oracle calls)."""
+
+from __future__ import annotations
+
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from oracle import moe_oracle as O
+from workloads.generate import ExpertWeights, shared_weights, to_f64
+
+# Layer output tolerance: max |err| <= 2e-2 * RMS(y_ref), mean |err| <= 2e-3 * RMS(y_ref)
+MAX_REL_RMS = 2e-2
+MEAN_REL_RMS = 2e-3
+# Routing end to end: tokens whose k-th / (k+1)-th score margin exceeds this
+# must route identically; router weights within 1e-3 absolute.
+MARGIN = 1e-3
+WEIGHT_ABS = 1e-3
+
+
+def assert_layer_close(y_gpu: np.ndarray, y_ref: np.ndarray, what: str = "y"):
+    y_gpu = np.asarray(y_gpu, dtype=np.float64)
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    assert y_gpu.shape == y_ref.shape, (y_gpu.shape, y_ref.shape)
+    rms = math.sqrt(float(np.mean(y_ref ** 2)))
+    err = np.abs(y_gpu - y_ref)
+    mx, mean = float(err.max()), float(err.mean())
+    assert rms > 0
+    assert mx <= MAX_REL_RMS * rms, f"{what}: max|err| {mx:.3e} > {MAX_REL_RMS} * rms {rms:.3e}"
+    assert mean <= MEAN_REL_RMS * rms, \
+        f"{what}: mean|err| {mean:.3e} > {MEAN_REL_RMS} * rms {rms:.3e}"
+    return mx / rms, mean / rms
+
+
+def score_margins(scores: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """Per token: score of the k-th chosen expert minus the best unchosen score
+    (inf when every expert is chosen)."""
+    T, k = idx.shape
+    E = scores.shape[1]
+    if k == E:
+        return np.full(T, np.inf)
+    m = np.empty(T)
+    for t in range(T):
+        chosen = set(int(e) for e in idx[t])
+        kth = scores[t, idx[t, k - 1]]
+        rest = max(scores[t, e] for e in range(E) if e not in chosen)
+        m[t] = kth - rest
+    return m
+
+
+def oracle_capacity(shape, T: Optional[int] = None) -> Optional[int]:
+    T = shape.T if T is None else T
+    return O.expert_capacity(T, shape.E, shape.capacity_factor)
+
+
+def oracle_layer(shape, inputs, tokens: Optional[Sequence[int]] = None):
+    """Run the float64 oracle on the (bf16/fp32) inputs, widened exactly."""
+    T = inputs["x"].shape[0]
+    return O.moe_layer_forward(
+        to_f64(inputs["x"]), to_f64(inputs["w_router"]),
+        ExpertWeights(inputs["w_gate"], inputs["w_up"], inputs["w_down"]),
+        k=shape.k, gate=shape.gate, renormalize=shape.renormalize,
+        routed_scaling_factor=shape.rsf, capacity=oracle_capacity(shape, T),
+        router_bias=to_f64(inputs["router_bias"]), shared=shared_weights(inputs),
+        tokens=tokens)
+
+
+def np_i(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy().astype(np.int64)
+
+
+def np_f(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu", torch.float64).numpy()

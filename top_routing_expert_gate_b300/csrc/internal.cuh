@@ -1,0 +1,127 @@
+// Internal declarations shared by the library's translation units.
+// Not part of the public ABI (that is include/moe_b300.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/moe_b300.h"
+
+namespace moe {
+
+// Device status word codes (first error wins; read by moe_get_error).
+enum DeviceStatus : int32_t {
+  kDevOk = 0,
+  kDevTimeout = 1,     // a bounded wait ran out
+  kDevBadIndex = 2,    // an index outside its valid range
+};
+
+__device__ __forceinline__ void record_error(int32_t* status, int32_t code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 32;
+constexpr int kTopkMaxBlocks = 4 * 148;   // partial sums of the mean probability
+constexpr int kDispatchChunk = 4096;      // assignments per dispatch block
+constexpr int kDispatchThreads = 1024;
+
+// Workspace layout: byte offsets from the workspace base, every region
+// 1024-byte aligned.  A single function computes it for the host side.
+struct WsLayout {
+  size_t status;      // int32 status word
+  size_t logits;      // [T, E] fp32
+  size_t mp_partial;  // [kTopkMaxBlocks, E] fp32
+  size_t topk_idx;    // [T, k] int32 (used when the caller passes no output)
+  size_t topk_w;      // [T, k] fp32
+  size_t counts;      // [E] int32
+  size_t drops;       // [E] int32
+  size_t offsets;     // [E + 1] int32
+  size_t mean_prob;   // [E] fp32
+  size_t block_hist;  // [nb, E] int32
+  size_t block_base;  // [nb, E] int32
+  size_t perm;        // [A] int32
+  size_t row_of;      // [A] int32
+  size_t drop_mask;   // [A] uint8
+  size_t x_perm;      // [A, d] act
+  size_t h;           // [A, F] act
+  size_t h_shared;    // [T, F_s] act
+  size_t y_perm;      // [A, d] fp32
+  size_t y_shared;    // [T, d] fp32
+  size_t total;
+  int nb;             // dispatch blocks
+};
+
+WsLayout ws_layout(const moe_config_t& c);
+
+inline size_t act_bytes(const moe_config_t& c) { return c.act_dtype == MOE_BF16 ? 2 : 4; }
+
+// Counts the library's own kernel launches of one call (for the benchmark's
+// launch accounting).
+struct LaunchCounter {
+  int n = 0;
+};
+inline void count_launch(LaunchCounter* lc, int k = 1) {
+  if (lc) lc->n += k;
+}
+
+// ---- launchers (each returns cudaGetLastError() after enqueueing) ----
+
+// Router logits z = x . W^T (+ bias), fp32 out [T, E].
+cudaError_t launch_router_logits(const moe_config_t& c, const void* x, const void* w_router,
+                                 const float* bias, float* logits, int32_t* status,
+                                 cudaStream_t s, LaunchCounter* lc = nullptr);
+
+// Gating + top-k from logits; mp_partial receives per-block partial sums of
+// the scores, then finalize writes mean_prob (may be null).
+cudaError_t launch_topk(const moe_config_t& c, const float* logits, int32_t* idx, float* w,
+                        float* mp_partial, float* mean_prob, cudaStream_t s,
+                        LaunchCounter* lc = nullptr);
+
+// Dispatch: histogram, scan, stable scatter.  row_of may be null.
+cudaError_t launch_dispatch(const moe_config_t& c, const int32_t* idx, int32_t* block_hist,
+                            int32_t* block_base, int32_t* counts, int32_t* drops,
+                            int32_t* offsets, int32_t* perm, int32_t* row_of,
+                            uint8_t* drop_mask, int32_t* status, cudaStream_t s,
+                            LaunchCounter* lc = nullptr);
+
+// x_perm[r] = x[perm[r] / k] for r < offsets[E].
+cudaError_t launch_gather(const moe_config_t& c, const void* x, const int32_t* perm,
+                          const int32_t* offsets, void* x_perm, int32_t* status,
+                          cudaStream_t s, LaunchCounter* lc = nullptr);
+
+// row_of[perm[r]] = r for r < offsets[E] (row_of pre-filled with -1).
+cudaError_t launch_invert_perm(const moe_config_t& c, const int32_t* perm,
+                               const int32_t* offsets, int32_t* row_of, int32_t* status,
+                               cudaStream_t s, LaunchCounter* lc = nullptr);
+
+// y[t] = sum_j kept g[t,j] y_perm[row_of[t*k+j]] (+ y_shared[t]).
+cudaError_t launch_combine(const moe_config_t& c, const float* y_perm, const float* topk_w,
+                           const int32_t* row_of, const uint8_t* drop_mask,
+                           const float* y_shared, void* y, int32_t* status, cudaStream_t s,
+                           LaunchCounter* lc = nullptr);
+
+// Grouped expert GEMMs.  Routed groups take rows offsets[e]..offsets[e+1] of
+// x_perm / h; the shared group (when ws_* given) takes all T rows of x / h_shared.
+struct ExpertArgs {
+  const void* x;        // [T, d]
+  const void* x_perm;   // [A, d]
+  const int32_t* offsets;
+  const void* w_gate; const void* w_up; const void* w_down;
+  const void* ws_gate; const void* ws_up; const void* ws_down;
+  void* h;              // [A, F]
+  void* h_shared;       // [T, F_s]
+  float* y_perm;        // [A, d]
+  float* y_shared;      // [T, d]
+  int32_t* status;
+  cudaEvent_t ev_up = nullptr;     // recorded before the gate/up GEMM when set
+  cudaEvent_t ev_down = nullptr;   // recorded before the down GEMM when set
+  LaunchCounter* launches = nullptr;
+};
+
+cudaError_t launch_experts_simt(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s);
+cudaError_t launch_experts_tc(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,406 @@
+// C ABI entry points (include/moe_b300.h): argument validation, workspace
+// layout and the stream-ordered launch sequence of the layer forward.
+#include "internal.cuh"
+
+#include <math.h>
+#include <string.h>
+
+namespace moe {
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+WsLayout ws_layout(const moe_config_t& c) {
+  WsLayout L{};
+  const size_t T = (size_t)c.T, E = (size_t)c.n_experts, k = (size_t)c.top_k;
+  const size_t d = (size_t)c.d_model, F = (size_t)c.d_ff, Fs = (size_t)c.d_ff_shared;
+  const size_t A = T * k;
+  const size_t ab = act_bytes(c);
+  L.nb = (int)((A + kDispatchChunk - 1) / kDispatchChunk);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + (bytes ? bytes : 1), 1024);
+    return at;
+  };
+  L.status = take(256);
+  L.logits = take(T * E * 4);
+  L.mp_partial = take((size_t)kTopkMaxBlocks * E * 4);
+  L.topk_idx = take(A * 4);
+  L.topk_w = take(A * 4);
+  L.counts = take(E * 4);
+  L.drops = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.mean_prob = take(E * 4);
+  L.block_hist = take((size_t)L.nb * E * 4);
+  L.block_base = take((size_t)L.nb * E * 4);
+  L.perm = take(A * 4);
+  L.row_of = take(A * 4);
+  L.drop_mask = take(A);
+  L.x_perm = take(A * d * ab);
+  L.h = take(A * F * ab);
+  L.h_shared = take(T * Fs * ab);
+  L.y_perm = take(A * d * 4);
+  L.y_shared = take(T * d * 4);
+  L.total = o;
+  return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+template <typename P>
+inline P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape/option checks shared by every call.
+moe_status_t check_config(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->d_model <= 0 || c->n_experts < 1 || c->top_k < 1 ||
+      c->top_k > c->n_experts || c->d_ff <= 0 || c->d_ff_shared < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->gate != MOE_GATE_SOFTMAX && c->gate != MOE_GATE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if ((c->act_dtype != MOE_BF16 && c->act_dtype != MOE_FP32) ||
+      (c->out_dtype != MOE_BF16 && c->out_dtype != MOE_FP32))
+    return MOE_ERR_INVALID_ARG;
+  if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_INVALID_ARG;
+  if (!isfinite(c->routed_scaling_factor)) return MOE_ERR_INVALID_ARG;
+  if ((long long)c->T * c->top_k > 0x7fffffffLL / 2) return MOE_ERR_INVALID_ARG;
+  if (c->n_experts > kMaxExperts || c->top_k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if (c->d_model % 4 != 0) return MOE_ERR_UNSUPPORTED;
+  if (c->act_dtype == MOE_BF16) {
+    if (c->d_model % 64 != 0 || c->d_ff % 128 != 0 || c->d_ff_shared % 128 != 0)
+      return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+moe_status_t check_ws(const moe_config_t* c, const void* ws, size_t ws_bytes) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < ws_layout(*c).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+// Required device pointer: non-null and 16-byte aligned (only when T > 0).
+bool bad_ptr(const moe_config_t* c, const void* p) {
+  if (c->T == 0) return false;
+  return p == nullptr || !aligned16(p);
+}
+// Optional device pointer: null or 16-byte aligned.
+bool bad_opt(const void* p) { return p != nullptr && !aligned16(p); }
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY_CUDA(expr)                         \
+  do {                                             \
+    cudaError_t _e = (expr);                       \
+    if (_e != cudaSuccess) return MOE_ERR_CUDA;    \
+  } while (0)
+
+#define MOE_TRY(expr)                              \
+  do {                                             \
+    moe_status_t _s = (expr);                      \
+    if (_s != MOE_OK) return _s;                   \
+  } while (0)
+
+cudaError_t run_experts(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s) {
+  if (c.act_dtype == MOE_BF16) return launch_experts_tc(c, a, s);
+  return launch_experts_simt(c, a, s);
+}
+
+moe_status_t check_shared_args(const moe_config_t* c, const void* g, const void* u,
+                               const void* d) {
+  const bool any = g || u || d;
+  const bool all = g && u && d;
+  if (any && !all) return MOE_ERR_INVALID_ARG;
+  if (all && c->d_ff_shared == 0) return MOE_ERR_INVALID_ARG;
+  if (!all && c->d_ff_shared > 0) return MOE_ERR_INVALID_ARG;
+  if (bad_opt(g) || bad_opt(u) || bad_opt(d)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_version(void) { return 100; }
+
+const char* moe_status_string(moe_status_t st) {
+  switch (st) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+int32_t moe_capacity(int32_t T, int32_t E, double capacity_factor) {
+  if (T < 0 || E <= 0 || !(capacity_factor >= 0.0)) return -1;
+  const double c = ceil(((double)T / (double)E) * capacity_factor);
+  if (c > 2147483647.0) return -1;
+  return (int32_t)c;
+}
+
+moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes) {
+  MOE_TRY(check_config(cfg));
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = ws_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_bytes,
+                                void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_TRY(check_ws(cfg, ws, ws_bytes));
+  const WsLayout L = ws_layout(*cfg);
+  return cuda_status(cudaMemsetAsync(at<char>(ws, L.status), 0, 256, (cudaStream_t)stream));
+}
+
+moe_status_t moe_topk_from_logits(const moe_config_t* cfg, const float* logits,
+                                  int32_t* topk_idx, float* topk_w, float* mean_prob,
+                                  void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_TRY(check_ws(cfg, ws, ws_bytes));
+  if (bad_ptr(cfg, logits) || bad_ptr(cfg, topk_idx) || bad_ptr(cfg, topk_w) ||
+      bad_opt(mean_prob))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*cfg);
+  return cuda_status(launch_topk(*cfg, logits, topk_idx, topk_w, at<float>(ws, L.mp_partial),
+                                 mean_prob, (cudaStream_t)stream));
+}
+
+moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x, const void* w_router,
+                             const float* router_bias, float* logits_out, int32_t* topk_idx,
+                             float* topk_w, float* mean_prob, void* ws, size_t ws_bytes,
+                             void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_TRY(check_ws(cfg, ws, ws_bytes));
+  if (bad_ptr(cfg, x) || bad_ptr(cfg, w_router) || bad_ptr(cfg, topk_idx) ||
+      bad_ptr(cfg, topk_w) || bad_opt(router_bias) || bad_opt(logits_out) || bad_opt(mean_prob))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*cfg);
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* status = at<int32_t>(ws, L.status);
+  float* z = logits_out ? logits_out : at<float>(ws, L.logits);
+  MOE_TRY_CUDA(launch_router_logits(*cfg, x, w_router, router_bias, z, status, s));
+  return cuda_status(
+      launch_topk(*cfg, z, topk_idx, topk_w, at<float>(ws, L.mp_partial), mean_prob, s));
+}
+
+moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* topk_idx, int32_t* counts,
+                          int32_t* drops, int32_t* offsets, int32_t* perm, uint8_t* drop_mask,
+                          void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_TRY(check_ws(cfg, ws, ws_bytes));
+  if (bad_ptr(cfg, topk_idx) || bad_ptr(cfg, perm) || bad_ptr(cfg, drop_mask) || !counts ||
+      !drops || !offsets || !aligned16(counts) || !aligned16(drops) || !aligned16(offsets))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*cfg);
+  return cuda_status(launch_dispatch(*cfg, topk_idx, at<int32_t>(ws, L.block_hist),
+                                     at<int32_t>(ws, L.block_base), counts, drops, offsets,
+                                     perm, nullptr, drop_mask, at<int32_t>(ws, L.status),
+                                     (cudaStream_t)stream));
+}
+
+moe_status_t moe_grouped_swiglu(const moe_config_t* cfg, const void* x, const int32_t* perm,
+                                const int32_t* offsets, const void* w_gate, const void* w_up,
+                                const void* w_down, const void* ws_gate, const void* ws_up,
+                                const void* ws_down, float* y_perm, float* y_shared, void* ws,
+                                size_t ws_bytes, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_TRY(check_ws(cfg, ws, ws_bytes));
+  if (bad_ptr(cfg, x) || bad_ptr(cfg, perm) || bad_ptr(cfg, w_gate) || bad_ptr(cfg, w_up) ||
+      bad_ptr(cfg, w_down) || bad_ptr(cfg, y_perm) || !offsets || !aligned16(offsets))
+    return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_shared_args(cfg, ws_gate, ws_up, ws_down));
+  if ((ws_gate != nullptr) != (y_shared != nullptr) || bad_opt(y_shared))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  const WsLayout L = ws_layout(*cfg);
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* status = at<int32_t>(ws, L.status);
+  void* x_perm = at<char>(ws, L.x_perm);
+  MOE_TRY_CUDA(launch_gather(*cfg, x, perm, offsets, x_perm, status, s));
+  ExpertArgs a{};
+  a.x = x;
+  a.x_perm = x_perm;
+  a.offsets = offsets;
+  a.w_gate = w_gate;
+  a.w_up = w_up;
+  a.w_down = w_down;
+  a.ws_gate = ws_gate;
+  a.ws_up = ws_up;
+  a.ws_down = ws_down;
+  a.h = at<char>(ws, L.h);
+  a.h_shared = at<char>(ws, L.h_shared);
+  a.y_perm = y_perm;
+  a.y_shared = y_shared;
+  a.status = status;
+  return cuda_status(run_experts(*cfg, a, s));
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const float* y_perm, const float* topk_w,
+                         const int32_t* offsets, const int32_t* perm,
+                         const uint8_t* drop_mask, const float* y_shared, void* y, void* ws,
+                         size_t ws_bytes, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_TRY(check_ws(cfg, ws, ws_bytes));
+  if (bad_ptr(cfg, y_perm) || bad_ptr(cfg, topk_w) || bad_ptr(cfg, perm) ||
+      bad_ptr(cfg, drop_mask) || bad_ptr(cfg, y) || !offsets || !aligned16(offsets) ||
+      bad_opt(y_shared))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  const WsLayout L = ws_layout(*cfg);
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* status = at<int32_t>(ws, L.status);
+  int32_t* row_of = at<int32_t>(ws, L.row_of);
+  MOE_TRY_CUDA(launch_invert_perm(*cfg, perm, offsets, row_of, status, s));
+  return cuda_status(
+      launch_combine(*cfg, y_perm, topk_w, row_of, drop_mask, y_shared, y, status, s));
+}
+
+}  // extern "C"
+
+namespace {
+
+// The layer forward.  When `ev` is non-null, ev[i] is recorded on the stream
+// before stage i (MOE_NUM_STAGES stages) and ev[MOE_NUM_STAGES] after the last.
+moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const void* w_router,
+                                const float* router_bias, const void* w_gate, const void* w_up,
+                                const void* w_down, const void* ws_gate, const void* ws_up,
+                                const void* ws_down, void* y, int32_t* topk_idx, float* topk_w,
+                                int32_t* counts, int32_t* drops, float* mean_prob, void* ws,
+                                size_t ws_bytes, void* stream, cudaEvent_t* ev,
+                                int32_t* n_launches) {
+  MOE_TRY(check_config(cfg));
+  MOE_TRY(check_ws(cfg, ws, ws_bytes));
+  if (bad_ptr(cfg, x) || bad_ptr(cfg, w_router) || bad_ptr(cfg, w_gate) ||
+      bad_ptr(cfg, w_up) || bad_ptr(cfg, w_down) || bad_ptr(cfg, y) || bad_opt(router_bias) ||
+      bad_opt(topk_idx) || bad_opt(topk_w) || bad_opt(counts) || bad_opt(drops) ||
+      bad_opt(mean_prob))
+    return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_shared_args(cfg, ws_gate, ws_up, ws_down));
+  const WsLayout L = ws_layout(*cfg);
+  cudaStream_t s = (cudaStream_t)stream;
+  const moe_config_t& c = *cfg;
+  LaunchCounter lc;
+  auto mark = [&](int i) -> cudaError_t {
+    return ev ? cudaEventRecord(ev[i], s) : cudaSuccess;
+  };
+  if (c.T == 0) {
+    if (counts) MOE_TRY_CUDA(cudaMemsetAsync(counts, 0, 4 * (size_t)c.n_experts, s));
+    if (drops) MOE_TRY_CUDA(cudaMemsetAsync(drops, 0, 4 * (size_t)c.n_experts, s));
+    if (mean_prob) MOE_TRY_CUDA(cudaMemsetAsync(mean_prob, 0, 4 * (size_t)c.n_experts, s));
+    for (int i = 0; ev && i <= MOE_NUM_STAGES; ++i) MOE_TRY_CUDA(mark(i));
+    if (n_launches) *n_launches = 0;
+    return MOE_OK;
+  }
+  int32_t* status = at<int32_t>(ws, L.status);
+  int32_t* idx = topk_idx ? topk_idx : at<int32_t>(ws, L.topk_idx);
+  float* g = topk_w ? topk_w : at<float>(ws, L.topk_w);
+  int32_t* cnt = counts ? counts : at<int32_t>(ws, L.counts);
+  int32_t* drp = drops ? drops : at<int32_t>(ws, L.drops);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* perm = at<int32_t>(ws, L.perm);
+  int32_t* row_of = at<int32_t>(ws, L.row_of);
+  uint8_t* dmask = at<uint8_t>(ws, L.drop_mask);
+  float* z = at<float>(ws, L.logits);
+
+  MOE_TRY_CUDA(mark(MOE_STAGE_ROUTER));
+  MOE_TRY_CUDA(launch_router_logits(c, x, w_router, router_bias, z, status, s, &lc));
+  MOE_TRY_CUDA(mark(MOE_STAGE_TOPK));
+  MOE_TRY_CUDA(launch_topk(c, z, idx, g, at<float>(ws, L.mp_partial), mean_prob, s, &lc));
+  MOE_TRY_CUDA(mark(MOE_STAGE_DISPATCH));
+  MOE_TRY_CUDA(launch_dispatch(c, idx, at<int32_t>(ws, L.block_hist),
+                               at<int32_t>(ws, L.block_base), cnt, drp, offsets, perm, row_of,
+                               dmask, status, s, &lc));
+  MOE_TRY_CUDA(mark(MOE_STAGE_GATHER));
+  void* x_perm = at<char>(ws, L.x_perm);
+  MOE_TRY_CUDA(launch_gather(c, x, perm, offsets, x_perm, status, s, &lc));
+  const bool has_shared = ws_gate != nullptr;
+  ExpertArgs a{};
+  a.x = x;
+  a.x_perm = x_perm;
+  a.offsets = offsets;
+  a.w_gate = w_gate;
+  a.w_up = w_up;
+  a.w_down = w_down;
+  a.ws_gate = ws_gate;
+  a.ws_up = ws_up;
+  a.ws_down = ws_down;
+  a.h = at<char>(ws, L.h);
+  a.h_shared = at<char>(ws, L.h_shared);
+  a.y_perm = at<float>(ws, L.y_perm);
+  a.y_shared = has_shared ? at<float>(ws, L.y_shared) : nullptr;
+  a.status = status;
+  a.ev_up = ev ? ev[MOE_STAGE_GATE_UP] : nullptr;
+  a.ev_down = ev ? ev[MOE_STAGE_DOWN] : nullptr;
+  a.launches = &lc;
+  MOE_TRY_CUDA(run_experts(c, a, s));
+  MOE_TRY_CUDA(mark(MOE_STAGE_COMBINE));
+  MOE_TRY_CUDA(launch_combine(c, a.y_perm, g, row_of, dmask, a.y_shared, y, status, s, &lc));
+  MOE_TRY_CUDA(mark(MOE_NUM_STAGES));
+  if (n_launches) *n_launches = lc.n;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const void* w_router,
+                               const float* router_bias, const void* w_gate, const void* w_up,
+                               const void* w_down, const void* ws_gate, const void* ws_up,
+                               const void* ws_down, void* y, int32_t* topk_idx, float* topk_w,
+                               int32_t* counts, int32_t* drops, float* mean_prob, void* ws,
+                               size_t ws_bytes, void* stream) {
+  return layer_forward_impl(cfg, x, w_router, router_bias, w_gate, w_up, w_down, ws_gate,
+                            ws_up, ws_down, y, topk_idx, topk_w, counts, drops, mean_prob, ws,
+                            ws_bytes, stream, nullptr, nullptr);
+}
+
+moe_status_t moe_layer_forward_profiled(const moe_config_t* cfg, const void* x,
+                                        const void* w_router, const float* router_bias,
+                                        const void* w_gate, const void* w_up,
+                                        const void* w_down, const void* ws_gate,
+                                        const void* ws_up, const void* ws_down, void* y,
+                                        int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                        int32_t* drops, float* mean_prob, void* ws,
+                                        size_t ws_bytes, void* stream, void** stage_events,
+                                        int32_t* n_launches) {
+  if (!stage_events) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i <= MOE_NUM_STAGES; ++i)
+    if (!stage_events[i]) return MOE_ERR_INVALID_ARG;
+  return layer_forward_impl(cfg, x, w_router, router_bias, w_gate, w_up, w_down, ws_gate,
+                            ws_up, ws_down, y, topk_idx, topk_w, counts, drops, mean_prob, ws,
+                            ws_bytes, stream, (cudaEvent_t*)stage_events, n_launches);
+}
+
+moe_status_t moe_get_error(const void* ws, void* stream) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t host = 0;
+  int32_t* dev = (int32_t*)ws;   // the status word is the first region (offset 0)
+  if (cudaMemcpyAsync(&host, dev, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (host != 0) {
+    if (cudaMemsetAsync(dev, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (host == kDevTimeout) return MOE_ERR_TIMEOUT;
+  if (host != 0) return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,255 @@
+// Router logits and the fused gating / top-k / renormalisation kernel.
+//
+// Method ("10. 混合专家 MoE：总参数与激活参数", niuwancheng.cn):
+//   logits = x . W_router^T                     (block sketch, first line)
+//   softmax  p_i = exp(z_i) / sum_j exp(z_j)    ("路由器怎样选专家：top-k 与两种门控")
+//   sigmoid  s_i = 1 / (1 + exp(-z_i))
+//   choose the k largest, renormalise over the chosen, times
+//   routed_scaling_factor (2.5 for DeepSeek-V3).
+// The selection compares the fp32 logits (softmax and sigmoid are increasing
+// in z) with ties going to the lower expert index.
+#include "internal.cuh"
+
+#include <math.h>
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// ---------------------------------------------------------------------------
+// Router logits, SIMT tiles of 64 tokens x 64 experts, fp32 accumulation.
+// ---------------------------------------------------------------------------
+template <typename TIn>
+__global__ void __launch_bounds__(256)
+router_logits_kernel(const TIn* __restrict__ x, const TIn* __restrict__ w,
+                     const float* __restrict__ bias, float* __restrict__ z,
+                     int T, int E, int d) {
+  __shared__ float As[32][64 + 1];
+  __shared__ float Bs[32][64 + 1];
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+
+  for (int k0 = 0; k0 < d; k0 += 32) {
+    for (int i = threadIdx.x; i < 64 * 32; i += 256) {
+      const int r = i >> 5, kk = i & 31;
+      const int gk = k0 + kk;
+      const int gm = m0 + r, gn = n0 + r;
+      As[kk][r] = (gm < T && gk < d) ? to_f(x[(size_t)gm * d + gk]) : 0.f;
+      Bs[kk][r] = (gn < E && gk < d) ? to_f(w[(size_t)gn * d + gk]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < 32; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx + 16 * j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int gm = m0 + ty + 16 * i;
+    if (gm >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int gn = n0 + tx + 16 * j;
+      if (gn < E) z[(size_t)gm * E + gn] = acc[i][j] + (bias ? bias[gn] : 0.f);
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// (za, ea) ranks before (zb, eb): larger logit, then lower expert index.
+__device__ __forceinline__ bool ranks_before(float za, int ea, float zb, int eb) {
+  return za > zb || (za == zb && ea < eb);
+}
+
+// ---------------------------------------------------------------------------
+// One warp per token.  Lane l holds experts l, l+32, ... (EPL per lane).
+// Block b owns tokens [b*tpb, (b+1)*tpb) so the mean-probability partial of
+// each block is a fixed-order sum, and the final reduction over blocks is too.
+// ---------------------------------------------------------------------------
+template <int EPL>
+__global__ void __launch_bounds__(256)
+topk_gate_kernel(const float* __restrict__ logits, int T, int E, int k, int gate,
+                 int renorm, float rsf, int tpb, int32_t* __restrict__ idx_out,
+                 float* __restrict__ w_out, float* __restrict__ mp_partial) {
+  __shared__ float red[8][kMaxExperts];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float acc[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
+
+  const int t_begin = blockIdx.x * tpb;
+  const int t_end = min(T, t_begin + tpb);
+  for (int t = t_begin + warp; t < t_end; t += 8) {
+    const float* row = logits + (size_t)t * E;
+    float zv[EPL], sc[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      zv[i] = e < E ? row[e] : -INFINITY;
+    }
+    if (gate == MOE_GATE_SOFTMAX) {
+      float m = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) m = fmaxf(m, zv[i]);
+      m = warp_max(m);
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        sc[i] = (lane + 32 * i < E) ? expf(zv[i] - m) : 0.f;
+        s += sc[i];
+      }
+      s = warp_sum(s);
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) sc[i] = sc[i] / s;
+    } else {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        sc[i] = (lane + 32 * i < E) ? 1.f / (1.f + expf(-zv[i])) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) acc[i] += sc[i];
+
+    unsigned selmask = 0;
+    int my_e = 0;
+    float my_s = 0.f;
+    for (int j = 0; j < k; ++j) {
+      float bz = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((selmask >> i) & 1u) && ranks_before(zv[i], e, bz, be)) {
+          bz = zv[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float oz = __shfl_xor_sync(0xffffffffu, bz, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (ranks_before(oz, oe, bz, be)) {
+          bz = oz;
+          be = oe;
+        }
+      }
+      const int owner = be & 31, slot = be >> 5;
+      float s_sel = 0.f;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (i == slot) s_sel = sc[i];
+      s_sel = __shfl_sync(0xffffffffu, s_sel, owner);
+      if (lane == owner) selmask |= 1u << slot;
+      if (lane == j) {
+        my_e = be;
+        my_s = s_sel;
+      }
+    }
+    float ssum = 0.f;
+    for (int j = 0; j < k; ++j) ssum += __shfl_sync(0xffffffffu, my_s, j);
+    if (lane < k) {
+      float g = renorm ? my_s / ssum : my_s;
+      g *= rsf;
+      idx_out[(size_t)t * k + lane] = my_e;
+      w_out[(size_t)t * k + lane] = g;
+    }
+  }
+  if (mp_partial == nullptr) return;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) red[warp][e] = acc[i];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) s += red[w][e];
+    mp_partial[(size_t)blockIdx.x * E + e] = s;
+  }
+}
+
+__global__ void mean_prob_finalize_kernel(const float* __restrict__ mp_partial, int nblocks,
+                                          int E, int T, float* __restrict__ mean_prob) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  float s = 0.f;
+  for (int b = 0; b < nblocks; ++b) s += mp_partial[(size_t)b * E + e];
+  mean_prob[e] = T > 0 ? s / (float)T : 0.f;
+}
+
+}  // namespace
+
+cudaError_t launch_router_logits(const moe_config_t& c, const void* x, const void* w_router,
+                                 const float* bias, float* logits, int32_t* status,
+                                 cudaStream_t s, LaunchCounter* lc) {
+  (void)status;
+  if (c.T == 0) return cudaSuccess;
+  dim3 grid((c.n_experts + 63) / 64, (c.T + 63) / 64);
+  if (c.act_dtype == MOE_BF16)
+    router_logits_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+        (const __nv_bfloat16*)x, (const __nv_bfloat16*)w_router, bias, logits, c.T,
+        c.n_experts, c.d_model);
+  else
+    router_logits_kernel<float><<<grid, 256, 0, s>>>((const float*)x, (const float*)w_router,
+                                                     bias, logits, c.T, c.n_experts, c.d_model);
+  count_launch(lc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const moe_config_t& c, const float* logits, int32_t* idx, float* w,
+                        float* mp_partial, float* mean_prob, cudaStream_t s,
+                        LaunchCounter* lc) {
+  const int T = c.T, E = c.n_experts;
+  if (T == 0) {
+    if (mean_prob) return cudaMemsetAsync(mean_prob, 0, sizeof(float) * E, s);
+    return cudaSuccess;
+  }
+  int nblocks = (T + 7) / 8;
+  if (nblocks > kTopkMaxBlocks) nblocks = kTopkMaxBlocks;
+  const int tpb = (T + nblocks - 1) / nblocks;
+  nblocks = (T + tpb - 1) / tpb;
+  float* part = mean_prob ? mp_partial : nullptr;
+#define MOE_TOPK_LAUNCH(EPL)                                                              \
+  topk_gate_kernel<EPL><<<nblocks, 256, 0, s>>>(logits, T, E, c.top_k, c.gate,          \
+                                                 c.renormalize, c.routed_scaling_factor, \
+                                                 tpb, idx, w, part)
+  if (E <= 32) MOE_TOPK_LAUNCH(1);
+  else if (E <= 64) MOE_TOPK_LAUNCH(2);
+  else if (E <= 128) MOE_TOPK_LAUNCH(4);
+  else MOE_TOPK_LAUNCH(8);
+#undef MOE_TOPK_LAUNCH
+  count_launch(lc);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess || !mean_prob) return err;
+  mean_prob_finalize_kernel<<<(E + 255) / 256, 256, 0, s>>>(mp_partial, nblocks, E, T, mean_prob);
+  count_launch(lc);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
