@@ -50,6 +50,21 @@ def score_margins(scores: np.ndarray, idx: np.ndarray) -> np.ndarray:
     return m
 
 
+def same_sets(gi: np.ndarray, ri: np.ndarray) -> np.ndarray:
+    """Per token: the chosen expert sets agree (order ignored)."""
+    return np.all(np.sort(gi, axis=1) == np.sort(ri, axis=1), axis=1)
+
+
+def order_separated(scores: np.ndarray, idx: np.ndarray, margin: float) -> np.ndarray:
+    """Per token: consecutive chosen scores differ by more than ``margin``, so
+    the order inside the chosen list is fixed too."""
+    T, k = idx.shape
+    if k == 1:
+        return np.ones(T, dtype=bool)
+    sel = np.take_along_axis(scores, idx, axis=1)
+    return np.all(sel[:, :-1] - sel[:, 1:] > margin, axis=1)
+
+
 def oracle_capacity(shape, T: Optional[int] = None) -> Optional[int]:
     T = shape.T if T is None else T
     return O.expert_capacity(T, shape.E, shape.capacity_factor)

@@ -1,7 +1,486 @@
-// placeholder: replaced by the tcgen05 grouped GEMM
-#include "internal.cuh"
+// Grouped SwiGLU expert GEMMs on the 5th-generation tensor cores (tcgen05,
+// sm_103a): the grouped GEMM that replaces the per-expert loop of the block
+// sketch in "10. 混合专家 MoE：总参数与激活参数" (niuwancheng.cn, "把一个大 FFN
+// 换成一组小 FFN": tokens routed to the same expert are gathered and
+// multiplied in one batch).
+//
+//   gate/up:  [g | u] = X_e [W_gate,e ; W_up,e]^T,  h = SiLU(g) * u  -> bf16
+//   down:     Y_e = h_e W_down,e^T                                   -> fp32
+//
+// Groups are the E routed experts (rows offsets[e]..offsets[e+1] of the
+// grouped activations) plus, when present, the shared expert (all T rows).
+// The tile list is derived on the device from `offsets`, so no host
+// synchronisation separates dispatch from the GEMMs.
+//
+// Kernel structure (one persistent CTA per SM, 192 threads):
+//   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per k-block
+//               (128-byte swizzle) into a 4-stage shared-memory ring;
+//   warp 1      allocates 512 TMEM columns; one thread issues
+//               tcgen05.mma M=128 N=256 K=16 into one of two 256-column fp32
+//               accumulators and commits stage / accumulator barriers;
+//   warps 2..5  epilogue: tcgen05.ld of its 32 TMEM lanes, SwiGLU (gate/up)
+//               or plain fp32 (down), 16-byte global stores.
+// For gate/up, the B tile's first 128 rows are W_gate rows and the next 128
+// the matching W_up rows, so one N=256 MMA produces both halves and the
+// SwiGLU pairs column j with column 128 + j of the same accumulator.
+#include "tc_common.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 namespace moe {
-cudaError_t launch_experts_tc(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s) {
-  return launch_experts_simt(c, a, s);
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128;
+constexpr int BK = 64;             // one 128-byte swizzle span of bf16
+constexpr int BN = 256;            // MMA N (gate/up: 128 gate + 128 up columns)
+constexpr int STAGES = 4;
+constexpr uint32_t A_STAGE = BM * BK * 2;   // 16 KB
+constexpr uint32_t B_STAGE = BN * BK * 2;   // 32 KB
+constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxGroups = kMaxExperts + 1;
+constexpr uint32_t kCtrlBytes = 256 + 4 * (kMaxGroups + 1 + 3 * kMaxGroups);
+constexpr uint32_t kSmemBytes = STAGES * (A_STAGE + B_STAGE) + kCtrlBytes + 1024;
+
+enum Mode { kGateUp = 0, kDown = 1 };
+
+struct TcParams {
+  CUtensorMap a_map[2];   // [0] routed grouped rows, [1] shared-expert rows
+  CUtensorMap b_map[2];   // gate (kGateUp) or down (kDown) weights
+  CUtensorMap u_map[2];   // up weights (kGateUp only)
+  const int32_t* offsets; // [E + 1]
+  void* out[2];
+  int ld_out[2];          // output row stride, elements
+  int K[2];               // reduction length per group kind
+  int N[2];               // output columns per group kind
+  int b_rows_per_expert;  // rows of one routed expert in b_map[0] / u_map[0]
+  int E, T, A;
+  int has_shared;
+  int32_t* status;
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ int n_tiles_of(int mode, int N) {
+  return mode == kGateUp ? N / 128 : (N + BN - 1) / BN;
 }
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t sA = base;
+  const uint32_t sB = base + STAGES * A_STAGE;
+  uint8_t* ctrl = smem + STAGES * (A_STAGE + B_STAGE);
+  const uint32_t bar0 = smem_u32(ctrl);
+  // barriers: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * STAGES + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 8 * (2 * STAGES + 5) + 4);
+  int* s_tile_start = reinterpret_cast<int*>(ctrl + 256);
+  int* s_row0 = s_tile_start + (kMaxGroups + 1);
+  int* s_rows = s_row0 + kMaxGroups;
+  int* s_mtiles = s_rows + kMaxGroups;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.E + (p.has_shared ? 1 : 0);
+  const int nt_r = n_tiles_of(MODE, p.N[0]);
+  const int nt_s = n_tiles_of(MODE, p.N[1]);
+
+  // ---- group table (rows per group, clamped to the grouped buffer) ----
+  for (int g = threadIdx.x; g < G; g += kThreads) {
+    int r0, rows;
+    if (g < p.E) {
+      r0 = min(max(p.offsets[g], 0), p.A);
+      rows = min(max(p.offsets[g + 1], r0), p.A) - r0;
+    } else {
+      r0 = 0;
+      rows = p.T;
+    }
+    s_row0[g] = r0;
+    s_rows[g] = rows;
+    s_mtiles[g] = (rows + BM - 1) / BM;
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&p.a_map[0]);
+    prefetch_tensormap(&p.b_map[0]);
+    if (MODE == kGateUp) prefetch_tensormap(&p.u_map[0]);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int s = 0;
+    for (int g = 0; g < G; ++g) {
+      s_tile_start[g] = s;
+      s += s_mtiles[g] * (g < p.E ? nt_r : nt_s);
+    }
+    s_tile_start[G] = s;
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = s_tile_start[G];
+
+  // tile t -> (group, m tile, n tile); m varies fastest so CTAs running at
+  // the same time share the weight tile (L2 reuse of the B operand).
+  auto decode = [&](int t, int& g, int& m, int& n) {
+    int lo = 0, hi = G;   // largest g with s_tile_start[g] <= t
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_tile_start[mid] <= t) lo = mid;
+      else hi = mid;
+    }
+    g = lo;
+    const int local = t - s_tile_start[g];
+    const int mt = s_mtiles[g];
+    n = local / mt;
+    m = local - n * mt;
+  };
+
+  bool failed = false;
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
+        int g, m, n;
+        decode(t, g, m, n);
+        const int kind = g < p.E ? 0 : 1;
+        const int nk = p.K[kind] / BK;
+        const int a_row = s_row0[g] + m * BM;
+        const int b_row = (kind ? 0 : g * p.b_rows_per_expert) + n * (MODE == kGateUp ? 128 : BN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
+            failed = true;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, STAGE_TX);
+          const uint32_t a_dst = sA + stage * A_STAGE;
+          const uint32_t b_dst = sB + stage * B_STAGE;
+          tma_load_2d(a_dst, &p.a_map[kind], fb, kb * BK, a_row);
+          if (MODE == kGateUp) {
+            tma_load_2d(b_dst, &p.b_map[kind], fb, kb * BK, b_row);
+            tma_load_2d(b_dst + B_STAGE / 2, &p.u_map[kind], fb, kb * BK, b_row);
+          } else {
+            tma_load_2d(b_dst, &p.b_map[kind], fb, kb * BK, b_row);
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (failed) {
+        *abort_flag = 1;
+        record_error(p.status, kDevTimeout);
+      }
+      // Never leave with copies in flight: wait (bounded) for the last
+      // phase armed on every stage.
+      for (int s = 0; s < STAGES; ++s) {
+        if (issued > s) {
+          const int armed = (issued - 1 - s) / STAGES + 1;
+          mbar_wait(full_bar(s), (uint32_t)((armed - 1) & 1), nullptr, p.timeout_ns);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x, ++local) {
+        int g, m, n;
+        decode(t, g, m, n);
+        const int kind = g < p.E ? 0 : 1;
+        const int nk = p.K[kind] / BK;
+        const int buf = local & 1;
+        const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
+        if (!mbar_wait(acce_bar(buf), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t a_desc = sdesc_k128(sA + stage * A_STAGE);
+          const uint64_t b_desc = sdesc_k128(sB + stage * B_STAGE);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // advance 16 bf16 = 32 bytes along K inside the swizzle span
+            mma_bf16(d_tmem, a_desc + (uint64_t)(2 * kk), b_desc + (uint64_t)(2 * kk), idesc,
+                     (kb | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (failed) break;
+        mma_commit(accf_bar(buf));
+      }
+      if (failed) {
+        *abort_flag = 1;
+        record_error(p.status, kDevTimeout);
+        // let every MMA already issued finish before the CTA tears down
+        mma_commit(drain_bar);
+        mbar_wait(drain_bar, 0, nullptr, p.timeout_ns);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int q = warp & 3;   // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    int local = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
+      int g, m, n;
+      decode(t, g, m, n);
+      const int kind = g < p.E ? 0 : 1;
+      const int buf = local & 1;
+      const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
+      if (!mbar_wait(accf_bar(buf), acc_phase, abort_flag, p.timeout_ns)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      const bool valid = m * BM + row < s_rows[g];
+      const size_t out_row = (size_t)(kind ? 0 : s_row0[g]) + (size_t)(m * BM + row);
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      if (MODE == kGateUp) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out[kind]) +
+                             out_row * (size_t)p.ld_out[kind] + (size_t)n * 128;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t gv[32], uv[32];
+          tmem_ld_32x32b_x32(tbase + (uint32_t)c, gv);
+          tmem_ld_32x32b_x32(tbase + 128u + (uint32_t)c, uv);
+          tmem_ld_wait();
+          if (valid) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float g0 = bits_f(gv[2 * j]), g1 = bits_f(gv[2 * j + 1]);
+              const float h0 = g0 / (1.f + __expf(-g0)) * bits_f(uv[2 * j]);
+              const float h1 = g1 / (1.f + __expf(-g1)) * bits_f(uv[2 * j + 1]);
+              __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
+              packed[j] = *reinterpret_cast<uint32_t*>(&hv);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
+                                  packed[4 * j + 3]);
+          }
+        }
+      } else {
+        float* out = reinterpret_cast<float*>(p.out[kind]) + out_row * (size_t)p.ld_out[kind] +
+                     (size_t)n * BN;
+        const int ncols = p.N[kind] - n * BN;   // > 0, a multiple of 64
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          if (c >= ncols) break;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + (uint32_t)c, v);
+          tmem_ld_wait();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(out + c);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_float4(bits_f(v[4 * j]), bits_f(v[4 * j + 1]), bits_f(v[4 * j + 2]),
+                                   bits_f(v[4 * j + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(buf));
+    }
+    if (failed) {
+      *abort_flag = 1;
+      if (lane == 0) record_error(p.status, kDevTimeout);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, inner] read in boxes of 64 x box_rows with the
+// 128-byte swizzle; rows past the end read as zero.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n = 148;
+  }
+  return n;
+}
+
+template <int MODE>
+cudaError_t launch(const TcParams& p, cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  grouped_gemm_kernel<MODE><<<num_sms(), kThreads, kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_experts_tc(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  const int T = c.T, E = c.n_experts, d = c.d_model, F = c.d_ff, Fs = c.d_ff_shared;
+  const int A = T * c.top_k;
+  const bool has_shared = Fs > 0 && a.ws_gate != nullptr;
+
+  TcParams p1{};
+  bool ok = true;
+  ok &= make_map(&p1.a_map[0], a.x_perm, d, A, BM);
+  ok &= make_map(&p1.a_map[1], a.x, d, T, BM);
+  ok &= make_map(&p1.b_map[0], a.w_gate, d, (uint64_t)E * F, 128);
+  ok &= make_map(&p1.u_map[0], a.w_up, d, (uint64_t)E * F, 128);
+  if (has_shared) {
+    ok &= make_map(&p1.b_map[1], a.ws_gate, d, Fs, 128);
+    ok &= make_map(&p1.u_map[1], a.ws_up, d, Fs, 128);
+  } else {
+    p1.b_map[1] = p1.b_map[0];
+    p1.u_map[1] = p1.u_map[0];
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  p1.offsets = a.offsets;
+  p1.out[0] = a.h;
+  p1.out[1] = a.h_shared;
+  p1.ld_out[0] = F;
+  p1.ld_out[1] = Fs;
+  p1.K[0] = d;
+  p1.K[1] = d;
+  p1.N[0] = F;
+  p1.N[1] = has_shared ? Fs : 128;
+  p1.b_rows_per_expert = F;
+  p1.E = E;
+  p1.T = T;
+  p1.A = A;
+  p1.has_shared = has_shared ? 1 : 0;
+  p1.status = a.status;
+  p1.timeout_ns = kWaitTimeoutNs;
+
+  TcParams p2 = p1;
+  ok = true;
+  ok &= make_map(&p2.a_map[0], a.h, F, A, BM);
+  ok &= make_map(&p2.b_map[0], a.w_down, F, (uint64_t)E * d, BN);
+  if (has_shared) {
+    ok &= make_map(&p2.a_map[1], a.h_shared, Fs, T, BM);
+    ok &= make_map(&p2.b_map[1], a.ws_down, Fs, d, BN);
+  } else {
+    p2.a_map[1] = p2.a_map[0];
+    p2.b_map[1] = p2.b_map[0];
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  p2.u_map[0] = p2.b_map[0];
+  p2.u_map[1] = p2.b_map[1];
+  p2.out[0] = a.y_perm;
+  p2.out[1] = a.y_shared;
+  p2.ld_out[0] = d;
+  p2.ld_out[1] = d;
+  p2.K[0] = F;
+  p2.K[1] = has_shared ? Fs : F;
+  p2.N[0] = d;
+  p2.N[1] = d;
+  p2.b_rows_per_expert = d;
+
+  if (a.ev_up) {
+    cudaError_t e = cudaEventRecord(a.ev_up, s);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t err = launch<kGateUp>(p1, s);
+  count_launch(a.launches);
+  if (err != cudaSuccess) return err;
+  if (a.ev_down) {
+    err = cudaEventRecord(a.ev_down, s);
+    if (err != cudaSuccess) return err;
+  }
+  err = launch<kDown>(p2, s);
+  count_launch(a.launches);
+  return err;
+}
+
 }  // namespace moe
