@@ -146,6 +146,33 @@ MOE_API moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* topk_i
                           int32_t* perm, uint8_t* drop_mask,
                           void* ws, size_t ws_bytes, void* stream);
 
+/* The same dispatch as moe_dispatch, for callers that cannot allocate device
+ * memory: no workspace argument, and nothing is allocated by this call.  The
+ * pages have no counterpart of this entry point; it exists for callers whose
+ * device memory is planned and owned by someone else (a host framework or
+ * runtime that fixes its memory arena when a model is loaded and rejects or
+ * cannot satisfy allocations afterwards, or a latency-critical serving loop
+ * where cudaMalloc/cudaFree would stall on the device), so neither they nor
+ * this library may call cudaMalloc to obtain a workspace.
+ *   - Scratch: the per-block tables live in a fixed 64 KiB device array built
+ *     into the library, held on every GPU that loads it until the process
+ *     exits.  Limit: T * top_k <= 131072 assignments (and n_experts <= 256);
+ *     larger batches return MOE_ERR_UNSUPPORTED without launching anything.
+ *   - The first call on each device looks up that array's device address
+ *     (cudaGetSymbolAddress) with that device current; make this first call
+ *     before any stream capture.
+ *   - All calls in the process share the one array: calls whose GPU work may
+ *     overlap (different streams, or different host threads on one device)
+ *     race on it and must be serialised by the caller.
+ *   - There is no status word: an expert index outside [0, E) is not counted
+ *     anywhere and its assignment is marked dropped, so sum(counts) +
+ *     sum(drops) < T * top_k reveals it.
+ * Arguments, outputs and determinism are those of moe_dispatch. */
+MOE_API moe_status_t moe_dispatch_no_workspace(const moe_config_t* cfg, const int32_t* topk_idx,
+                                               int32_t* counts, int32_t* drops,
+                                               int32_t* offsets, int32_t* perm,
+                                               uint8_t* drop_mask, void* stream);
+
 /* Grouped SwiGLU experts over dispatched rows (the grouped GEMM that replaces
  * the block sketch's per-expert loop).  Row r < offsets[E] of the grouped
  * batch is token perm[r] / k and belongs to the expert whose segment holds r:

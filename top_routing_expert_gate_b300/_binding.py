@@ -67,6 +67,8 @@ SIGNATURES = {
                                        c_void_p, c_size_t, c_void_p]),
     "moe_dispatch": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                c_void_p, c_void_p, c_size_t, c_void_p]),
+    "moe_dispatch_no_workspace": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p,
+                                            c_void_p, c_void_p, c_void_p]),
     "moe_grouped_swiglu": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_void_p, c_size_t, c_void_p]),

@@ -16,6 +16,8 @@
 // lane rank), so every output is a pure function of topk_idx.
 #include "internal.cuh"
 
+#include <mutex>
+
 namespace moe {
 namespace {
 
@@ -334,3 +336,80 @@ cudaError_t launch_combine(const moe_config_t& c, const float* y_perm, const flo
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Dispatch without a caller-provided workspace.
+//
+// The two per-block tables the dispatch kernels need (histogram and running
+// base, each [blocks, E] int32) live in one fixed device array compiled into
+// this library instead of in the caller's workspace.  Every GPU that loads
+// the library holds this array (64 KiB) until the process exits.  Host code
+// cannot use the array's name as a device address, so its address is looked
+// up once per device with cudaGetSymbolAddress and then passed to the
+// kernels like any other pointer.
+// ---------------------------------------------------------------------------
+namespace moe {
+namespace {
+
+constexpr int kStaticDispatchBlocks = 32;   // 32 x 4096 = 131072 assignments
+constexpr int kStaticScratchInts = 2 * kStaticDispatchBlocks * kMaxExperts;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) int32_t g_dispatch_scratch[kStaticScratchInts];
+
+std::mutex g_scratch_mu;
+int32_t* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_dispatch_scratch on the current device (looked up on
+// the first call per device).
+cudaError_t static_scratch(int32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+bool aligned16_ptr(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_dispatch_no_workspace(const moe_config_t* cfg,
+                                                  const int32_t* topk_idx, int32_t* counts,
+                                                  int32_t* drops, int32_t* offsets,
+                                                  int32_t* perm, uint8_t* drop_mask,
+                                                  void* stream) {
+  using namespace moe;
+  if (!cfg) return MOE_ERR_INVALID_ARG;
+  const moe_config_t& c = *cfg;
+  if (c.T < 0 || c.n_experts < 1 || c.top_k < 1 || c.top_k > c.n_experts)
+    return MOE_ERR_INVALID_ARG;
+  if (c.n_experts > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  const long long A = (long long)c.T * c.top_k;
+  if (A > (long long)kStaticDispatchBlocks * kDispatchChunk) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !drops || !offsets || !aligned16_ptr(counts) || !aligned16_ptr(drops) ||
+      !aligned16_ptr(offsets))
+    return MOE_ERR_INVALID_ARG;
+  if (A > 0 && (!topk_idx || !perm || !drop_mask || !aligned16_ptr(topk_idx) ||
+                !aligned16_ptr(perm) || !aligned16_ptr(drop_mask)))
+    return MOE_ERR_INVALID_ARG;
+  int32_t* scratch = nullptr;
+  if (static_scratch(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  // Both tables are fully written before they are read (histogram, then
+  // running base), so nothing has to be cleared between calls.
+  int32_t* block_hist = scratch;
+  int32_t* block_base = scratch + kStaticDispatchBlocks * kMaxExperts;
+  const cudaError_t e = launch_dispatch(c, topk_idx, block_hist, block_base, counts, drops,
+                                        offsets, perm, nullptr, drop_mask, nullptr,
+                                        (cudaStream_t)stream);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
