@@ -69,16 +69,45 @@ inline void count_launch(LaunchCounter* lc, int k = 1) {
 
 // ---- launchers (each returns cudaGetLastError() after enqueueing) ----
 
-// Router logits z = x . W^T (+ bias), fp32 out [T, E].
-cudaError_t launch_router_logits(const moe_config_t& c, const void* x, const void* w_router,
-                                 const float* bias, float* logits, int32_t* status,
-                                 cudaStream_t s, LaunchCounter* lc = nullptr);
+// fp32 router logits held as `splits` partial sums [splits][T][E] plus an
+// optional per-expert bias: z[t,e] = sum_s partials[s][t][e] (in s order) + bias[e].
+struct LogitsView {
+  const float* partials;
+  int splits;
+  size_t split_stride;   // elements from one partial to the next
+  const float* bias;     // nullable
+};
 
-// Gating + top-k from logits; mp_partial receives per-block partial sums of
-// the scores, then finalize writes mean_prob (may be null).
-cudaError_t launch_topk(const moe_config_t& c, const float* logits, int32_t* idx, float* w,
-                        float* mp_partial, float* mean_prob, cudaStream_t s,
-                        LaunchCounter* lc = nullptr);
+// Tensor-core router: one 128-token tile per CTA, reduction over d split
+// across CTAs when there are few token tiles (at most kRouterCtaTarget CTAs
+// unless T alone needs more).
+constexpr int kRouterCtaTarget = 160;
+constexpr int kMaxRouterSplits = 16;
+struct RouterPlan {
+  int m_tiles, kb_total, kb_per, splits;
+};
+RouterPlan plan_router(const moe_config_t& c);
+// Floats of scratch the router needs for its partial sums.
+inline size_t router_scratch_floats(const moe_config_t& c) {
+  const size_t rows = (size_t)c.T > (size_t)kRouterCtaTarget * 128 ? (size_t)c.T
+                                                                     : (size_t)kRouterCtaTarget * 128;
+  return rows * (size_t)c.n_experts;
+}
+
+// Router logits of x . W^T (+ bias) into `scratch`; describes them in *view.
+cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_router,
+                          const float* bias, float* scratch, LogitsView* view, int32_t* status,
+                          cudaStream_t s, LaunchCounter* lc = nullptr);
+cudaError_t launch_router_tc(const moe_config_t& c, const void* x, const void* w_router,
+                             float* partial, int32_t* status, cudaStream_t s,
+                             LaunchCounter* lc = nullptr);
+
+// Gating + top-k from logits; writes the summed logits to logits_out when
+// given; mp_partial receives per-block partial sums of the scores, then a
+// finalize kernel writes mean_prob (may be null).
+cudaError_t launch_topk(const moe_config_t& c, const LogitsView& z, float* logits_out,
+                        int32_t* idx, float* w, float* mp_partial, float* mean_prob,
+                        cudaStream_t s, LaunchCounter* lc = nullptr);
 
 // Dispatch: histogram, scan, stable scatter.  row_of may be null.
 cudaError_t launch_dispatch(const moe_config_t& c, const int32_t* idx, int32_t* block_hist,

@@ -23,7 +23,7 @@ WsLayout ws_layout(const moe_config_t& c) {
     return at;
   };
   L.status = take(256);
-  L.logits = take(T * E * 4);
+  L.logits = take(router_scratch_floats(c) * 4);
   L.mp_partial = take((size_t)kTopkMaxBlocks * E * 4);
   L.topk_idx = take(A * 4);
   L.topk_w = take(A * 4);
@@ -175,8 +175,9 @@ moe_status_t moe_topk_from_logits(const moe_config_t* cfg, const float* logits,
       bad_opt(mean_prob))
     return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(*cfg);
-  return cuda_status(launch_topk(*cfg, logits, topk_idx, topk_w, at<float>(ws, L.mp_partial),
-                                 mean_prob, (cudaStream_t)stream));
+  const LogitsView view{logits, 1, 0, nullptr};
+  return cuda_status(launch_topk(*cfg, view, nullptr, topk_idx, topk_w,
+                                 at<float>(ws, L.mp_partial), mean_prob, (cudaStream_t)stream));
 }
 
 moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x, const void* w_router,
@@ -191,10 +192,11 @@ moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x, const void*
   const WsLayout L = ws_layout(*cfg);
   cudaStream_t s = (cudaStream_t)stream;
   int32_t* status = at<int32_t>(ws, L.status);
-  float* z = logits_out ? logits_out : at<float>(ws, L.logits);
-  MOE_TRY_CUDA(launch_router_logits(*cfg, x, w_router, router_bias, z, status, s));
-  return cuda_status(
-      launch_topk(*cfg, z, topk_idx, topk_w, at<float>(ws, L.mp_partial), mean_prob, s));
+  LogitsView view{};
+  MOE_TRY_CUDA(launch_router(*cfg, x, w_router, router_bias, at<float>(ws, L.logits), &view,
+                             status, s));
+  return cuda_status(launch_topk(*cfg, view, logits_out, topk_idx, topk_w,
+                                 at<float>(ws, L.mp_partial), mean_prob, s));
 }
 
 moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* topk_idx, int32_t* counts,
@@ -317,9 +319,11 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
   float* z = at<float>(ws, L.logits);
 
   MOE_TRY_CUDA(mark(MOE_STAGE_ROUTER));
-  MOE_TRY_CUDA(launch_router_logits(c, x, w_router, router_bias, z, status, s, &lc));
+  LogitsView view{};
+  MOE_TRY_CUDA(launch_router(c, x, w_router, router_bias, z, &view, status, s, &lc));
   MOE_TRY_CUDA(mark(MOE_STAGE_TOPK));
-  MOE_TRY_CUDA(launch_topk(c, z, idx, g, at<float>(ws, L.mp_partial), mean_prob, s, &lc));
+  MOE_TRY_CUDA(launch_topk(c, view, nullptr, idx, g, at<float>(ws, L.mp_partial), mean_prob, s,
+                           &lc));
   MOE_TRY_CUDA(mark(MOE_STAGE_DISPATCH));
   MOE_TRY_CUDA(launch_dispatch(c, idx, at<int32_t>(ws, L.block_hist),
                                at<int32_t>(ws, L.block_base), cnt, drp, offsets, perm, row_of,

@@ -94,8 +94,9 @@ __device__ __forceinline__ bool ranks_before(float za, int ea, float zb, int eb)
 // ---------------------------------------------------------------------------
 template <int EPL>
 __global__ void __launch_bounds__(256)
-topk_gate_kernel(const float* __restrict__ logits, int T, int E, int k, int gate,
-                 int renorm, float rsf, int tpb, int32_t* __restrict__ idx_out,
+topk_gate_kernel(const float* __restrict__ partials, int splits, size_t split_stride,
+                 const float* __restrict__ bias, float* __restrict__ logits_out, int T, int E,
+                 int k, int gate, int renorm, float rsf, int tpb, int32_t* __restrict__ idx_out,
                  float* __restrict__ w_out, float* __restrict__ mp_partial) {
   __shared__ float red[8][kMaxExperts];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -106,12 +107,20 @@ topk_gate_kernel(const float* __restrict__ logits, int T, int E, int k, int gate
   const int t_begin = blockIdx.x * tpb;
   const int t_end = min(T, t_begin + tpb);
   for (int t = t_begin + warp; t < t_end; t += 8) {
-    const float* row = logits + (size_t)t * E;
+    const float* row = partials + (size_t)t * E;
     float zv[EPL], sc[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = lane + 32 * i;
-      zv[i] = e < E ? row[e] : -INFINITY;
+      if (e < E) {
+        float v = row[e];
+        for (int sp = 1; sp < splits; ++sp) v += row[(size_t)sp * split_stride + e];
+        if (bias) v += bias[e];
+        zv[i] = v;
+        if (logits_out) logits_out[(size_t)t * E + e] = v;
+      } else {
+        zv[i] = -INFINITY;
+      }
     }
     if (gate == MOE_GATE_SOFTMAX) {
       float m = -INFINITY;
@@ -205,26 +214,34 @@ __global__ void mean_prob_finalize_kernel(const float* __restrict__ mp_partial, 
 
 }  // namespace
 
-cudaError_t launch_router_logits(const moe_config_t& c, const void* x, const void* w_router,
-                                 const float* bias, float* logits, int32_t* status,
-                                 cudaStream_t s, LaunchCounter* lc) {
-  (void)status;
-  if (c.T == 0) return cudaSuccess;
+cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_router,
+                          const float* bias, float* scratch, LogitsView* view, int32_t* status,
+                          cudaStream_t s, LaunchCounter* lc) {
+  view->partials = scratch;
+  view->split_stride = (size_t)c.T * c.n_experts;
+  if (c.T == 0) {
+    view->splits = 1;
+    view->bias = nullptr;
+    return cudaSuccess;
+  }
+  if (c.act_dtype == MOE_BF16) {
+    // tensor cores; the bias is added where the partial sums are combined
+    view->splits = plan_router(c).splits;
+    view->bias = bias;
+    return launch_router_tc(c, x, w_router, scratch, status, s, lc);
+  }
+  view->splits = 1;
+  view->bias = nullptr;
   dim3 grid((c.n_experts + 63) / 64, (c.T + 63) / 64);
-  if (c.act_dtype == MOE_BF16)
-    router_logits_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-        (const __nv_bfloat16*)x, (const __nv_bfloat16*)w_router, bias, logits, c.T,
-        c.n_experts, c.d_model);
-  else
-    router_logits_kernel<float><<<grid, 256, 0, s>>>((const float*)x, (const float*)w_router,
-                                                     bias, logits, c.T, c.n_experts, c.d_model);
+  router_logits_kernel<float><<<grid, 256, 0, s>>>((const float*)x, (const float*)w_router, bias,
+                                                   scratch, c.T, c.n_experts, c.d_model);
   count_launch(lc);
   return cudaGetLastError();
 }
 
-cudaError_t launch_topk(const moe_config_t& c, const float* logits, int32_t* idx, float* w,
-                        float* mp_partial, float* mean_prob, cudaStream_t s,
-                        LaunchCounter* lc) {
+cudaError_t launch_topk(const moe_config_t& c, const LogitsView& z, float* logits_out,
+                        int32_t* idx, float* w, float* mp_partial, float* mean_prob,
+                        cudaStream_t s, LaunchCounter* lc) {
   const int T = c.T, E = c.n_experts;
   if (T == 0) {
     if (mean_prob) return cudaMemsetAsync(mean_prob, 0, sizeof(float) * E, s);
@@ -236,9 +253,10 @@ cudaError_t launch_topk(const moe_config_t& c, const float* logits, int32_t* idx
   nblocks = (T + tpb - 1) / tpb;
   float* part = mean_prob ? mp_partial : nullptr;
 #define MOE_TOPK_LAUNCH(EPL)                                                              \
-  topk_gate_kernel<EPL><<<nblocks, 256, 0, s>>>(logits, T, E, c.top_k, c.gate,          \
-                                                 c.renormalize, c.routed_scaling_factor, \
-                                                 tpb, idx, w, part)
+  topk_gate_kernel<EPL><<<nblocks, 256, 0, s>>>(z.partials, z.splits, z.split_stride,   \
+                                                 z.bias, logits_out, T, E, c.top_k,      \
+                                                 c.gate, c.renormalize,                  \
+                                                 c.routed_scaling_factor, tpb, idx, w, part)
   if (E <= 32) MOE_TOPK_LAUNCH(1);
   else if (E <= 64) MOE_TOPK_LAUNCH(2);
   else if (E <= 128) MOE_TOPK_LAUNCH(4);
