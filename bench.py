@@ -60,6 +60,9 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--experts", type=int, default=None,
+                    help="profiling aid: keep the workload's per-expert GEMM shapes but use "
+                         "this many experts (tokens scaled to keep rows per expert)")
     return ap.parse_args(argv)
 
 
@@ -242,6 +245,11 @@ def main(argv=None):
     from workloads import SHAPES, make_inputs
 
     shape = SHAPES[args.workload]
+    if args.experts is not None and args.experts != shape.E:
+        from dataclasses import replace
+        T = max(1, shape.T * args.experts // shape.E)
+        shape = replace(shape, name=f"{shape.name}_E{args.experts}", E=args.experts,
+                        k=min(shape.k, args.experts), T=T)
 
     if args.impl == "reference":
         if rank != 0:
@@ -257,7 +265,7 @@ def main(argv=None):
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": 1e3 * t, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
+                "config": {"workload": WORKLOAD_TEXT[args.workload], "name": shape.name},
                 "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores_used(),
                                  "kind": "oracle",
                                  "sample": f"per step: routing of all {shape.T} tokens + layer "
@@ -402,7 +410,7 @@ def main(argv=None):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": shape.dtype,
         "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": shape.name,
                    "global_batch_tokens": world * T, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2: every step streams "
                          f"{work['weight_bytes'] / 1e9:.2f} GB of expert weights (L2 126 MB)",
