@@ -222,6 +222,23 @@ def time_oracle(shape, inputs, sample_tokens: int, steps: int, warmup: int = 0):
     return times
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest ``value`` over all ranks (the slowest replica sets the time);
+    ``value`` itself when not running distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def tokens_per_second(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
+
+
 def cores_used():
     try:
         return len(os.sched_getaffinity(0))
@@ -339,11 +356,7 @@ def main(argv=None):
     if world > 1:
         dist.barrier()
     clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = tt.item()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
     ms_per_step = total_ms / args.steps
     status = moe.moe_get_error(ws)
     if status != 0:
@@ -372,11 +385,7 @@ def main(argv=None):
         y_host.copy_(y, non_blocking=True)
     e2e_end.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e2e_start.elapsed_time(e2e_end) / args.e2e_steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = tt.item()
+    e2e_ms = max_over_ranks(e2e_start.elapsed_time(e2e_end) / args.e2e_steps, dev)
 
     if rank != 0:
         if world > 1:
@@ -404,7 +413,7 @@ def main(argv=None):
                 "peak_source": f"hbm_gbs ({peak_src})"}
     roof["traffic"] = stored_traffic(args.workload, dom)
 
-    value = world * T / (ms_per_step * 1e-3)
+    value = tokens_per_second(T, world, ms_per_step)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -422,7 +431,7 @@ def main(argv=None):
         "roofline": roof,
         "gpu_launches": launches,
         "clocks": clocks.summary(),
-        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": tokens_per_second(T, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": x.numel() * x.element_size(),
                 "d2h_bytes_per_step": y.numel() * y.element_size()},
     }

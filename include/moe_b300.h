@@ -239,6 +239,17 @@ MOE_API moe_status_t moe_layer_forward_profiled(
     int32_t* counts, int32_t* drops, float* mean_prob, void* ws, size_t ws_bytes, void* stream,
     void** stage_events, int32_t* n_launches);
 
+/* Self-test of the device-side failure detection.  Every wait inside the
+ * library's tensor-core kernels is bounded; when a bound runs out the kernel
+ * records MOE_ERR_TIMEOUT in the workspace status word, drains its own copies
+ * in flight, frees its tensor memory and returns instead of hanging.  This
+ * call launches one tiny kernel whose single bounded wait can never be
+ * satisfied, with the given bound (1 ns .. 1 s), so that a caller can check
+ * that moe_get_error then reports MOE_ERR_TIMEOUT and that the CUDA context
+ * stays usable.  `ws` is any workspace (only its status word is used). */
+MOE_API moe_status_t moe_selftest_bounded_wait(void* ws, size_t ws_bytes, uint64_t timeout_ns,
+                                               void* stream);
+
 /* Synchronises `stream`, reads and clears the workspace status word.
  * Returns MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (or MOE_ERR_CUDA if the
  * stream itself reports an error). */

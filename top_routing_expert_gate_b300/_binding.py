@@ -84,6 +84,7 @@ SIGNATURES = {
                                              c_void_p, c_void_p, c_size_t, c_void_p, c_void_p,
                                              c_void_p]),
     "moe_get_error": (c_int32, [c_void_p, c_void_p]),
+    "moe_selftest_bounded_wait": (c_int32, [c_void_p, c_size_t, ctypes.c_uint64, c_void_p]),
 }
 
 _lib = None
