@@ -58,8 +58,11 @@ MID_SHAPES = {
 }
 
 
+@pytest.mark.parametrize("layout", ["tokens_m", "weights_m"])
 @pytest.mark.parametrize("name", list(MID_SHAPES))
-def test_layer_matches_oracle_all_tokens(name):
+def test_layer_matches_oracle_all_tokens(name, layout, monkeypatch):
+    # both tile layouts of the bf16 grouped GEMMs (tokens or weights in the MMA's M)
+    monkeypatch.setenv("MOE_B300_EXPERT_LAYOUT", layout)
     s = MID_SHAPES[name]
     inp = make_inputs(s, device=DEV, seed=1)
     cfg, out = _run_layer(s, inp)

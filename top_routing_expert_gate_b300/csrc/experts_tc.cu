@@ -299,8 +299,8 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const float g0 = bits_f(gv[2 * j]), g1 = bits_f(gv[2 * j + 1]);
-              const float h0 = g0 / (1.f + __expf(-g0)) * bits_f(uv[2 * j]);
-              const float h1 = g1 / (1.f + __expf(-g1)) * bits_f(uv[2 * j + 1]);
+              const float h0 = silu_f(g0) * bits_f(uv[2 * j]);
+              const float h1 = silu_f(g1) * bits_f(uv[2 * j + 1]);
               __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
               packed[j] = *reinterpret_cast<uint32_t*>(&hv);
             }
@@ -508,45 +508,6 @@ router_gemm_kernel(const __grid_constant__ RouterParams p) {
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-// Row-major bf16 matrix [rows, inner] read in boxes of 64 x box_rows with the
-// 128-byte swizzle; rows past the end read as zero.
-bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      n = 148;
-  }
-  return n;
-}
 
 template <int MODE>
 cudaError_t launch(const TcParams& p, cudaStream_t s) {

@@ -152,5 +152,8 @@ struct ExpertArgs {
 
 cudaError_t launch_experts_simt(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s);
 cudaError_t launch_experts_tc(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s);
+// The same GEMMs with the expert weights in the MMA's M and the tokens in N
+// (token tiles of any multiple of 16 rows, so ragged experts pad little).
+cudaError_t launch_experts_wm(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s);
 
 }  // namespace moe
