@@ -19,7 +19,8 @@
 //               tcgen05.mma M=128 N=256 K=16 into one of two 256-column fp32
 //               accumulators and commits stage / accumulator barriers;
 //   warps 2..5  epilogue: tcgen05.ld of its 32 TMEM lanes, SwiGLU (gate/up)
-//               or plain fp32 (down), 16-byte global stores.
+//               or plain fp32 (down), transposed through shared memory so
+//               that each global store writes whole row segments.
 // For gate/up, the B tile's first 128 rows are W_gate rows and the next 128
 // the matching W_up rows, so one N=256 MMA produces both halves and the
 // SwiGLU pairs column j with column 128 + j of the same accumulator.
@@ -45,7 +46,12 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxGroups = kMaxExperts + 1;
 constexpr uint32_t kCtrlBytes = 256 + 4 * (kMaxGroups + 1 + 3 * kMaxGroups);
-constexpr uint32_t kSmemBytes = STAGES * (A_STAGE + B_STAGE) + kCtrlBytes + 1024;
+// Epilogue staging: per epilogue warp, 32 rows x 33 words (one word of
+// padding keeps both the row-wise writes and the column-wise reads free of
+// bank conflicts).
+constexpr uint32_t kStageWords = 32 * 33;
+constexpr uint32_t kEpiBytes = 4 * kStageWords * 4;
+constexpr uint32_t kSmemBytes = STAGES * (A_STAGE + B_STAGE) + kEpiBytes + kCtrlBytes + 1024;
 
 enum Mode { kGateUp = 0, kDown = 1 };
 
@@ -78,7 +84,8 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t sA = base;
   const uint32_t sB = base + STAGES * A_STAGE;
-  uint8_t* ctrl = smem + STAGES * (A_STAGE + B_STAGE);
+  uint32_t* epi_stage = reinterpret_cast<uint32_t*>(smem + STAGES * (A_STAGE + B_STAGE));
+  uint8_t* ctrl = smem + STAGES * (A_STAGE + B_STAGE) + kEpiBytes;
   const uint32_t bar0 = smem_u32(ctrl);
   // barriers: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -269,7 +276,6 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     const int q = warp & 3;   // TMEM lane quarter this warp may access
-    const int row = q * 32 + lane;
     int local = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
       int g, m, n;
@@ -282,38 +288,42 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
         break;
       }
       tc_fence_after();
-      const bool valid = m * BM + row < s_rows[g];
-      const size_t out_row = (size_t)(kind ? 0 : s_row0[g]) + (size_t)(m * BM + row);
+      // Each thread holds one row of the tile (TMEM lane) for 32 columns per
+      // load.  The warp passes its 32 x 32 block through shared memory so
+      // that every global store writes contiguous bytes of one or two rows.
+      const int rows_left = s_rows[g] - (m * BM + q * 32);   // valid rows of this warp's block
+      const size_t row_base = (size_t)(kind ? 0 : s_row0[g]) + (size_t)(m * BM + q * 32);
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      uint32_t* st = epi_stage + q * kStageWords;
       if (MODE == kGateUp) {
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out[kind]) +
-                             out_row * (size_t)p.ld_out[kind] + (size_t)n * 128;
+        uint32_t* out = reinterpret_cast<uint32_t*>(p.out[kind]);   // bf16 pairs
+        const size_t ld2 = (size_t)p.ld_out[kind] / 2;
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
           uint32_t gv[32], uv[32];
           tmem_ld_32x32b_x32(tbase + (uint32_t)c, gv);
           tmem_ld_32x32b_x32(tbase + 128u + (uint32_t)c, uv);
           tmem_ld_wait();
-          if (valid) {
-            uint32_t packed[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float g0 = bits_f(gv[2 * j]), g1 = bits_f(gv[2 * j + 1]);
-              const float h0 = silu_f(g0) * bits_f(uv[2 * j]);
-              const float h1 = silu_f(g1) * bits_f(uv[2 * j + 1]);
-              __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
-              packed[j] = *reinterpret_cast<uint32_t*>(&hv);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(out + c);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
-                                  packed[4 * j + 3]);
+          for (int j = 0; j < 16; ++j) {
+            const float h0 = silu_f(bits_f(gv[2 * j])) * bits_f(uv[2 * j]);
+            const float h1 = silu_f(bits_f(gv[2 * j + 1])) * bits_f(uv[2 * j + 1]);
+            __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
+            st[lane * 33 + j] = *reinterpret_cast<uint32_t*>(&hv);
           }
+          __syncwarp();
+          // two rows of 64 bytes per store: lanes 0..15 row r, lanes 16..31 row r + 1
+          const size_t col2 = ((size_t)n * 128 + (size_t)c) / 2 + (size_t)(lane & 15);
+#pragma unroll 4
+          for (int r = 0; r < 32; r += 2) {
+            const int rr = r + (lane >> 4);
+            if (rr < rows_left) out[(row_base + rr) * ld2 + col2] = st[rr * 33 + (lane & 15)];
+          }
+          __syncwarp();
         }
       } else {
-        float* out = reinterpret_cast<float*>(p.out[kind]) + out_row * (size_t)p.ld_out[kind] +
-                     (size_t)n * BN;
+        float* out = reinterpret_cast<float*>(p.out[kind]);
+        const size_t ld = (size_t)p.ld_out[kind];
         const int ncols = p.N[kind] - n * BN;   // > 0, a multiple of 64
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
@@ -321,13 +331,15 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tbase + (uint32_t)c, v);
           tmem_ld_wait();
-          if (valid) {
-            float4* dst = reinterpret_cast<float4*>(out + c);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              dst[j] = make_float4(bits_f(v[4 * j]), bits_f(v[4 * j + 1]), bits_f(v[4 * j + 2]),
-                                   bits_f(v[4 * j + 3]));
-          }
+          for (int j = 0; j < 32; ++j) st[lane * 33 + j] = v[j];
+          __syncwarp();
+          // one row of 128 bytes per store
+          const size_t col = (size_t)n * BN + (size_t)c + (size_t)lane;
+#pragma unroll 4
+          for (int r = 0; r < 32; ++r)
+            if (r < rows_left) out[(row_base + r) * ld + col] = bits_f(st[r * 33 + lane]);
+          __syncwarp();
         }
       }
       tc_fence_before();

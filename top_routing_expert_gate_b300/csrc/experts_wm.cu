@@ -8,28 +8,35 @@
 //   gate/up:  h_e = SiLU(X_e W_gate,e^T) * (X_e W_up,e^T)   -> bf16
 //   down:     Y_e = h_e W_down,e^T                          -> fp32
 //
-// computed transposed, D^T = W . X^T: the 128 MMA rows (TMEM lanes) are
-// output features of one expert and the MMA's N columns are that expert's
-// tokens.  tcgen05 takes any N that is a multiple of 16 up to 256, so an
-// expert with R rows is covered by ceil(R / 256) token tiles of
-// round16(R / tiles) columns each: the padding is below 16 rows per tile,
-// where 128-row token tiles waste up to 127 (about a quarter of the work when
-// every expert holds ~256 rows, as in the DeepSeek-V3-shaped layer).
+// computed transposed, D^T = W . X^T: MMA rows (TMEM lanes) are output
+// features of one expert and the MMA's N columns are that expert's tokens.
+// tcgen05 takes any N that is a multiple of 16 up to 256, so an expert with
+// R rows is covered by ceil(R / 256) token tiles of round32(R / tiles)
+// columns each: the padding is below 32 rows per tile, where 128-row token
+// tiles waste up to 127 (about a fifth of the work when every expert holds
+// ~256 rows, as in the DeepSeek-V3-shaped layer).
 //
-// Kernel structure (one persistent CTA per SM, 192 threads):
-//   warp 0      TMA producer: a 128x64 weight tile (gate/up: 64 W_gate rows
-//               over the 64 matching W_up rows) and an Nx64 token tile
-//               (N <= 256, loaded as 128/64/32/16-row boxes) per k-block, with
-//               the 128-byte swizzle, into a 4-stage shared-memory ring;
-//   warp 1      allocates 512 TMEM columns; one thread issues
-//               tcgen05.mma M=128 N=N K=16 into one of two 256-column fp32
-//               accumulators;
-//   warps 2..5  epilogue: tcgen05.ld of its 32 TMEM lanes (= 32 features for
-//               32 tokens per load).  Gate/up: the warps holding W_gate lanes
-//               and those holding the matching W_up lanes swap half of their
-//               tokens through shared memory, then each applies SiLU(g)*u to
+// Two CTAs (a cluster pair, on two SMs) share one M = 256 MMA
+// (tcgen05 .cta_group::2): each CTA stages its own 128 weight rows and half
+// of the tile's tokens, so a pipeline stage costs each CTA 32 KB instead of
+// 48 KB and six stages fit in shared memory.
+//
+// Per CTA (192 threads, one per SM, persistent over pair tiles):
+//   warp 0      TMA producer: 128x64 weight tile (gate/up: 64 W_gate rows
+//               over the 64 matching W_up rows) + (N/2)x64 token rows per
+//               k-block, 128-byte swizzle, 6-stage ring; every copy of both
+//               CTAs completes on the even CTA's stage barrier;
+//   warp 1      allocates 512 TMEM columns (pair allocation); in the even CTA
+//               one thread issues tcgen05.mma.cta_group::2 M=256 N=N K=16
+//               into one of two 256-column fp32 accumulators and multicasts
+//               stage-free / accumulator-full commits to both CTAs;
+//   warps 2..5  epilogue on this CTA's 128 lanes (= 128 features, all N
+//               tokens).  Gate/up: the warps holding W_gate lanes and those
+//               holding the matching W_up lanes swap half of each 32-token
+//               chunk through shared memory, then each applies SiLU(g)*u to
 //               16 tokens and stores bf16 h; down: every warp stores its fp32
-//               features.
+//               features.  They release the accumulator on the even CTA's
+//               barrier.
 #include "tc_common.cuh"
 
 namespace moe {
@@ -37,12 +44,13 @@ namespace {
 
 using namespace tc;
 
-constexpr int WM = 128;             // MMA M: weight rows per tile
+constexpr int WM = 128;             // weight rows per CTA (MMA M = 256 per pair)
 constexpr int WBK = 64;             // k-block: one 128-byte swizzle span of bf16
-constexpr int TN = 256;             // maximum token columns per tile (MMA N)
-constexpr int WSTAGES = 4;
-constexpr uint32_t W_STAGE = WM * WBK * 2;   // 16 KB
-constexpr uint32_t T_STAGE = TN * WBK * 2;   // 32 KB
+constexpr int TN = 256;             // maximum token columns per pair tile (MMA N)
+constexpr int TNH = TN / 2;         // token rows staged by each CTA
+constexpr int WSTAGES = 6;
+constexpr uint32_t W_STAGE = WM * WBK * 2;    // 16 KB
+constexpr uint32_t T_STAGE = TNH * WBK * 2;   // 16 KB
 constexpr int kWThreads = 192;
 constexpr uint32_t kWTmemCols = 512;
 constexpr int kWMaxGroups = kMaxExperts + 1;
@@ -71,7 +79,8 @@ struct WmParams {
   uint64_t timeout_ns;
 };
 
-__device__ __forceinline__ int feat_per_tile(int mode) { return mode == kWGateUp ? 64 : WM; }
+// output features of one pair tile (half of them in each CTA)
+__device__ __forceinline__ int feat_per_tile(int mode) { return mode == kWGateUp ? 128 : 2 * WM; }
 
 // Named barrier 1 over the four epilogue warps (128 threads).
 __device__ __forceinline__ void epi_bar_sync() {
@@ -103,7 +112,8 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
   float* xchg = reinterpret_cast<float*>(smem + WSTAGES * (W_STAGE + T_STAGE));
   uint8_t* ctrl = smem + WSTAGES * (W_STAGE + T_STAGE) + kXchgBytes;
   const uint32_t bar0 = smem_u32(ctrl);
-  // barriers: full[WSTAGES], empty[WSTAGES], acc_full[2], acc_empty[2], drain
+  // barriers: full[WSTAGES], empty[WSTAGES], acc_full[2], acc_empty[2], drain.
+  // full and acc_empty are used in the even CTA only.
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (WSTAGES + s); };
   auto accf_bar = [&](int b) { return bar0 + 8u * (2 * WSTAGES + b); };
@@ -115,15 +125,17 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
   int* s_row0 = s_tile_start + (kWMaxGroups + 1);
   int* s_rows = s_row0 + kWMaxGroups;
   int* s_ntok = s_rows + kWMaxGroups;    // token tiles of the group
-  int* s_tsize = s_ntok + kWMaxGroups;   // token rows per tile (multiple of 16)
+  int* s_tsize = s_ntok + kWMaxGroups;   // token rows per tile (multiple of 32)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();   // 0: issues the MMAs; 1: its peer
+  const int pair = (int)cluster_id_x(), npairs = (int)nclusters_x();
   const int G = p.E + (p.has_shared ? 1 : 0);
   const int fpt = feat_per_tile(MODE);
   const int nf_r = (p.n_feat[0] + fpt - 1) / fpt;
   const int nf_s = (p.n_feat[1] + fpt - 1) / fpt;
 
-  // ---- group table: rows, token tiling ----
+  // ---- group table: rows, token tiling (identical in both CTAs) ----
   for (int g = threadIdx.x; g < G; g += kWThreads) {
     int r0, rows;
     if (g < p.E) {
@@ -134,9 +146,9 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
       rows = p.T;
     }
     int nt = (rows + TN - 1) / TN;
-    int ts = 16;
+    int ts = 32;
     if (nt > 0) {
-      ts = ((rows + nt - 1) / nt + 15) & ~15;   // <= TN
+      ts = ((rows + nt - 1) / nt + 31) & ~31;   // <= TN
       nt = (rows + ts - 1) / ts;
     }
     s_row0[g] = r0;
@@ -151,7 +163,7 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 4);
+      mbar_init(acce_bar(b), 8);   // four epilogue warps in each CTA
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -163,8 +175,8 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
     prefetch_tensormap(&p.t_map[0][0]);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kWTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(tmem_slot), kWTmemCols);
+    tmem_relinquish_pair();
     tc_fence_before();
   }
   __syncthreads();
@@ -176,14 +188,15 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
     }
     s_tile_start[G] = s;
   }
-  __syncthreads();
+  // both CTAs' barriers exist before any copy or commit targets them
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = s_tile_start[G];
 
-  // tile t -> (group, feature tile f, token tile j); j varies fastest so the
-  // CTAs that share a weight tile run at the same time (L2 reuse), and the
-  // token tiles of one expert stay in L2 while its feature tiles stream.
+  // pair tile t -> (group, feature tile f, token tile j); j varies fastest so
+  // the pairs that share a weight tile run at the same time (L2 reuse), and
+  // the token tiles of one expert stay in L2 while its feature tiles stream.
   auto decode = [&](int t, int& g, int& f, int& j) {
     int lo = 0, hi = G;   // largest g with s_tile_start[g] <= t
     while (hi - lo > 1) {
@@ -197,50 +210,52 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
     f = local / nt;
     j = local - f * nt;
   };
-  // token rows of tile j of group g, and the MMA N that covers them
+  // token rows of tile j of group g, and the MMA N (a multiple of 32) covering them
   auto tile_rows = [&](int g, int j, int& first, int& rows, int& n) {
     const int ts = s_tsize[g];
     first = j * ts;
     rows = min(ts, s_rows[g] - first);
-    n = (rows + 15) & ~15;
+    n = (rows + 31) & ~31;
   };
 
   bool failed = false;
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer ----------------
+      // ---------------- TMA producer (both CTAs) ----------------
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
-      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
+      for (int t = pair; t < total && !failed; t += npairs) {
         int g, f, j, first, rows, n;
         decode(t, g, f, j);
         tile_rows(g, j, first, rows, n);
         const int kind = g < p.E ? 0 : 1;
         const int nk = p.K[kind] / WBK;
-        const int w_row = (kind ? 0 : g * p.w_rows_per_expert) + f * fpt;
-        const int t_row = s_row0[g] + first;
-        const uint32_t tx = W_STAGE + (uint32_t)n * (WBK * 2);
+        const int half = n >> 1;   // token rows staged by this CTA, multiple of 16
+        const int w_row = (kind ? 0 : g * p.w_rows_per_expert) + f * fpt + (int)rank * (fpt / 2);
+        const int t_row = s_row0[g] + first + (int)rank * half;
+        const uint32_t tx_pair = 2u * (W_STAGE + (uint32_t)half * (WBK * 2));
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
             failed = true;
             break;
           }
-          const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, tx);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), tx_pair);
+          const uint32_t fb = mapa_shared(full_bar(stage), 0);
           const uint32_t w_dst = sW + stage * W_STAGE;
           const uint32_t t_dst = sT + stage * T_STAGE;
-          tma_load_2d(w_dst, &p.w_map[kind], fb, kb * WBK, w_row);
-          if (MODE == kWGateUp) tma_load_2d(w_dst + W_STAGE / 2, &p.u_map[kind], fb, kb * WBK, w_row);
+          tma_load_2d_pair(w_dst, &p.w_map[kind], fb, kb * WBK, w_row);
+          if (MODE == kWGateUp)
+            tma_load_2d_pair(w_dst + W_STAGE / 2, &p.u_map[kind], fb, kb * WBK, w_row);
           // token rows as boxes of 128, 64, 32, 16; every box starts on a
           // 16-row (2 KB) boundary, so the swizzle pattern is that of one tile
           int off = 0;
 #pragma unroll
           for (int b = 0; b < kTokBoxes; ++b) {
             const int box = 128 >> b;
-            while (n - off >= box) {
-              tma_load_2d(t_dst + (uint32_t)off * (WBK * 2), &p.t_map[kind][b], fb, kb * WBK,
-                          t_row + off);
+            while (half - off >= box) {
+              tma_load_2d_pair(t_dst + (uint32_t)off * (WBK * 2), &p.t_map[kind][b], fb,
+                               kb * WBK, t_row + off);
               off += box;
             }
           }
@@ -255,38 +270,40 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
         *abort_flag = 1;
         record_error(p.status, kDevTimeout);
       }
-      // Never leave with copies in flight: wait (bounded) for the last
-      // phase armed on every stage.
-      for (int s = 0; s < WSTAGES; ++s) {
-        if (issued > s) {
-          const int armed = (issued - 1 - s) / WSTAGES + 1;
-          mbar_wait(full_bar(s), (uint32_t)((armed - 1) & 1), nullptr, p.timeout_ns);
+      // Never leave with copies in flight: the even CTA waits (bounded) for
+      // the last phase armed on every stage, which counts both CTAs' bytes.
+      if (rank == 0) {
+        for (int s = 0; s < WSTAGES; ++s) {
+          if (issued > s) {
+            const int armed = (issued - 1 - s) / WSTAGES + 1;
+            mbar_wait_cluster(full_bar(s), (uint32_t)((armed - 1) & 1), nullptr, p.timeout_ns);
+          }
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (even CTA) ----------------
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
-      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x, ++local) {
+      for (int t = pair; t < total && !failed; t += npairs, ++local) {
         int g, f, j, first, rows, n;
         decode(t, g, f, j);
         tile_rows(g, j, first, rows, n);
         const int kind = g < p.E ? 0 : 1;
         const int nk = p.K[kind] / WBK;
-        const uint32_t idesc = idesc_bf16_f32(WM, (uint32_t)n);
+        const uint32_t idesc = idesc_bf16_f32(2 * WM, (uint32_t)n);
         const int buf = local & 1;
         const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
-        if (!mbar_wait(acce_bar(buf), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
+        if (!mbar_wait_cluster(acce_bar(buf), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
           failed = true;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * TN);
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
+          if (!mbar_wait_cluster(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
             failed = true;
             break;
           }
@@ -296,39 +313,41 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
 #pragma unroll
           for (int kk = 0; kk < WBK / 16; ++kk) {
             // advance 16 bf16 = 32 bytes along K inside the swizzle span
-            mma_bf16(d_tmem, a_desc + (uint64_t)(2 * kk), b_desc + (uint64_t)(2 * kk), idesc,
-                     (kb | kk) != 0 ? 1u : 0u);
+            mma_bf16_pair(d_tmem, a_desc + (uint64_t)(2 * kk), b_desc + (uint64_t)(2 * kk), idesc,
+                          (kb | kk) != 0 ? 1u : 0u);
           }
-          mma_commit(empty_bar(stage));
+          mma_commit_pair_mc(empty_bar(stage), 3);
           if (++stage == WSTAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (failed) break;
-        mma_commit(accf_bar(buf));
+        mma_commit_pair_mc(accf_bar(buf), 3);
       }
       if (failed) {
         *abort_flag = 1;
         record_error(p.status, kDevTimeout);
-        // let every MMA already issued finish before the CTA tears down
-        mma_commit(drain_bar);
+        // let every MMA already issued finish before the pair tears down
+        mma_commit_pair(drain_bar);
         mbar_wait(drain_bar, 0, nullptr, p.timeout_ns);
       }
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+    // ---------------- epilogue (warps 2..5, both CTAs) ----------------
     const int q = warp & 3;   // TMEM lane quarter this warp may access
+    const uint32_t lead_acce0 = mapa_shared(acce_bar(0), 0);
+    const uint32_t lead_acce1 = mapa_shared(acce_bar(1), 0);
     int local = 0;
     uint32_t chunk_no = 0;    // running count of exchange chunks (buffer parity)
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
+    for (int t = pair; t < total; t += npairs, ++local) {
       int g, f, j, first, rows, n;
       decode(t, g, f, j);
       tile_rows(g, j, first, rows, n);
       const int kind = g < p.E ? 0 : 1;
       const int buf = local & 1;
       const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
-      const bool ok = mbar_wait(accf_bar(buf), acc_phase, abort_flag, p.timeout_ns);
+      const bool ok = mbar_wait_cluster(accf_bar(buf), acc_phase, abort_flag, p.timeout_ns);
       if (MODE == kWGateUp) {
         // the exchange below synchronises the four warps, so all of them
         // must take the same decision on whether to process the tile
@@ -343,16 +362,17 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * TN);
       const size_t row0 = (size_t)(kind ? 0 : s_row0[g]) + (size_t)first;
+      const int feat0 = f * fpt + (int)rank * (fpt / 2);   // this CTA's first feature
       if (MODE == kWGateUp) {
-        // lanes 0..63: gate features f*64 + 0..63; lanes 64..127: the same up
+        // lanes 0..63: gate features feat0 + 0..63; lanes 64..127: the same up
         // features.  Per 32-token chunk the gate warps hand their values of
         // tokens 16..31 to the up warps and receive the up values of tokens
         // 0..15, so each of the four warps finishes 16 tokens.
         const bool is_gate = q < 2;
-        const int fl = (q & 1) * 32 + lane;   // feature within the tile
+        const int fl = (q & 1) * 32 + lane;   // feature within this CTA's 64
         const int tok0 = is_gate ? 0 : 16;    // tokens of the chunk this warp finishes
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out[kind]) +
-                             row0 * p.ld_out[kind] + (size_t)(f * 64 + fl);
+                             row0 * p.ld_out[kind] + (size_t)(feat0 + fl);
 #pragma unroll 1
         for (int c = 0; c < n; c += 32, ++chunk_no) {
           float* xb = xchg + (chunk_no & 1u) * (32 * 64);
@@ -376,7 +396,7 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
           }
         }
       } else {
-        const int feat = f * WM + q * 32 + lane;
+        const int feat = feat0 + q * 32 + lane;
         const bool fvalid = feat < p.n_feat[kind];
         float* out = reinterpret_cast<float*>(p.out[kind]) + row0 * p.ld_out[kind] + feat;
 #pragma unroll 1
@@ -394,7 +414,7 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce_bar(buf));
+      if (lane == 0) mbar_arrive_cluster(buf ? lead_acce1 : lead_acce0);
     }
     if (failed) {
       *abort_flag = 1;
@@ -404,9 +424,12 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
 
   tc_fence_before();
   __syncthreads();
+  // neither CTA leaves (or frees tensor memory) while its peer may still
+  // read its shared memory or signal its barriers
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kWTmemCols);
+    tmem_dealloc_pair(tmem_base, kWTmemCols);
   }
 }
 
@@ -414,13 +437,45 @@ template <int MODE>
 cudaError_t launch_wm(const WmParams& p, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
+  static int pairs = 0;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(grouped_gemm_wm_kernel<MODE>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmemBytes);
+    if (attr_err != cudaSuccess) return;
+    // as many co-resident pairs as the device holds (at most one CTA per SM)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    cfg.blockDim = dim3(kWThreads);
+    cfg.dynamicSmemBytes = kWSmemBytes;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_wm_kernel<MODE>, &cfg) != cudaSuccess ||
+        n <= 0) {
+      (void)cudaGetLastError();
+      n = num_sms() / 2;
+    }
+    pairs = n < num_sms() / 2 ? n : num_sms() / 2;
   });
   if (attr_err != cudaSuccess) return attr_err;
-  grouped_gemm_wm_kernel<MODE><<<num_sms(), kWThreads, kWSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(kWThreads);
+  cfg.dynamicSmemBytes = kWSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_wm_kernel<MODE>, p);
 }
 
 bool token_maps(CUtensorMap (&m)[kTokBoxes], const void* ptr, uint64_t inner, uint64_t rows) {
