@@ -583,7 +583,8 @@ cudaError_t launch_router_tc(const moe_config_t& c, const void* x, const void* w
   return cudaGetLastError();
 }
 
-cudaError_t launch_experts_tc(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s) {
+cudaError_t launch_gemm_tc(const moe_config_t& c, const ExpertArgs& a, int which,
+                           cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
   const int T = c.T, E = c.n_experts, d = c.d_model, F = c.d_ff, Fs = c.d_ff_shared;
   const int A = T * c.top_k;
@@ -644,18 +645,7 @@ cudaError_t launch_experts_tc(const moe_config_t& c, const ExpertArgs& a, cudaSt
   p2.N[1] = d;
   p2.b_rows_per_expert = d;
 
-  if (a.ev_up) {
-    cudaError_t e = cudaEventRecord(a.ev_up, s);
-    if (e != cudaSuccess) return e;
-  }
-  cudaError_t err = launch<kGateUp>(p1, s);
-  count_launch(a.launches);
-  if (err != cudaSuccess) return err;
-  if (a.ev_down) {
-    err = cudaEventRecord(a.ev_down, s);
-    if (err != cudaSuccess) return err;
-  }
-  err = launch<kDown>(p2, s);
+  cudaError_t err = which == kGemmGateUp ? launch<kGateUp>(p1, s) : launch<kDown>(p2, s);
   count_launch(a.launches);
   return err;
 }

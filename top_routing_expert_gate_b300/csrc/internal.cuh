@@ -145,15 +145,20 @@ struct ExpertArgs {
   float* y_perm;        // [A, d]
   float* y_shared;      // [T, d]
   int32_t* status;
-  cudaEvent_t ev_up = nullptr;     // recorded before the gate/up GEMM when set
-  cudaEvent_t ev_down = nullptr;   // recorded before the down GEMM when set
+  cudaEvent_t ev_up = nullptr;     // recorded before the gate/up GEMM when set (fp32 path)
+  cudaEvent_t ev_down = nullptr;   // recorded before the down GEMM when set (fp32 path)
   LaunchCounter* launches = nullptr;
 };
 
 cudaError_t launch_experts_simt(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s);
-cudaError_t launch_experts_tc(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s);
-// The same GEMMs with the expert weights in the MMA's M and the tokens in N
-// (token tiles of any multiple of 16 rows, so ragged experts pad little).
-cudaError_t launch_experts_wm(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s);
+// One of the two bf16 grouped GEMMs (kGemmGateUp: x -> h, kGemmDown: h -> y),
+// in one of two tile layouts:
+//   _tc: tokens in the MMA's M (128-row token tiles, 256 weight rows per tile);
+//   _wm: expert weights in M and tokens in N, on CTA pairs (token tiles of any
+//        multiple of 32 rows, so ragged experts pad little).
+constexpr int kGemmGateUp = 0;
+constexpr int kGemmDown = 1;
+cudaError_t launch_gemm_tc(const moe_config_t& c, const ExpertArgs& a, int which, cudaStream_t s);
+cudaError_t launch_gemm_wm(const moe_config_t& c, const ExpertArgs& a, int which, cudaStream_t s);
 
 }  // namespace moe

@@ -110,21 +110,32 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
     if (_s != MOE_OK) return _s;                   \
   } while (0)
 
-// Tile layout of the bf16 grouped GEMMs.  Tokens in the MMA's M (128-row
-// token tiles, 256 weight rows per tile) suit experts that hold many rows;
-// weights in M with tokens in N (token tiles of any multiple of 16 up to 256)
-// pad ragged experts far less.  MOE_B300_EXPERT_LAYOUT=tokens_m|weights_m
-// overrides the choice (for tests and tuning).
-bool weights_in_m(const moe_config_t& c) {
+// Tile layout of each bf16 grouped GEMM: true = expert weights in the MMA's
+// M (launch_gemm_wm), false = tokens in M (launch_gemm_tc).
+// MOE_B300_EXPERT_LAYOUT=tokens_m|weights_m|mixed overrides the choice for
+// tests and tuning (mixed: weights in M for gate/up, tokens in M for down).
+bool weights_in_m(const moe_config_t& c, int which) {
+  (void)c;
   const char* o = getenv("MOE_B300_EXPERT_LAYOUT");
   if (o && strcmp(o, "tokens_m") == 0) return false;
   if (o && strcmp(o, "weights_m") == 0) return true;
+  if (o && strcmp(o, "mixed") == 0) return which == kGemmGateUp;
   return false;
 }
 
 cudaError_t run_experts(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s) {
   if (c.act_dtype != MOE_BF16) return launch_experts_simt(c, a, s);
-  return weights_in_m(c) ? launch_experts_wm(c, a, s) : launch_experts_tc(c, a, s);
+  for (int which = kGemmGateUp; which <= kGemmDown; ++which) {
+    cudaEvent_t ev = which == kGemmGateUp ? a.ev_up : a.ev_down;
+    if (ev) {
+      const cudaError_t e = cudaEventRecord(ev, s);
+      if (e != cudaSuccess) return e;
+    }
+    const cudaError_t e = weights_in_m(c, which) ? launch_gemm_wm(c, a, which, s)
+                                                 : launch_gemm_tc(c, a, which, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 moe_status_t check_shared_args(const moe_config_t* c, const void* g, const void* u,
