@@ -19,7 +19,9 @@ Readings taken where the pages are silent (each is listed in the design doc):
   * top-k ties go to the lower expert index; the chosen list is ordered by
     logit descending, then index ascending;
   * the selection key is the raw logit z (softmax and sigmoid are strictly
-    increasing in z, so the chosen set is the one the pages describe);
+    increasing in z, so the chosen set is the one the pages describe); with a
+    DeepSeek-V3 score bias or expert groups it is s + b, as the pages state;
+  * the bias step leaves an expert exactly at the mean load unchanged;
   * routed_scaling_factor multiplies the routed weights only; the shared
     expert is added with weight 1;
   * capacity = ceil((T / E) * capacity_factor) in IEEE double; slots are
@@ -127,6 +129,68 @@ def topk_weights(scores: np.ndarray, idx: np.ndarray, renormalize: bool,
     return g * routed_scaling_factor
 
 
+# ---------------------------------------------------------------------------
+# DeepSeek-V3 auxiliary-loss-free selection ([moe10] "DeepSeek-V3 的无辅助损失
+# 偏置"; [routing] the paragraph on auxiliary-loss-free load balancing).  Each
+# expert carries a bias b_e that enters only the ranking, s_e + b_e; the
+# combine weights keep the raw score s_e.  With groups, the experts are split
+# into n_group equal consecutive groups, a group is scored by the sum of its
+# two best ranking values, the topk_group best groups are kept, and the k
+# experts are chosen among the kept groups only (node-limited routing: a token
+# reaches at most topk_group groups).
+# ---------------------------------------------------------------------------
+
+def group_scores(keys: np.ndarray, n_group: int) -> np.ndarray:
+    """score[t, g] = the two largest keys[t, e] of group g, added."""
+    keys = np.asarray(keys, dtype=np.float64)
+    T, E = keys.shape
+    if n_group < 1 or E % n_group != 0 or E // n_group < 2:
+        raise ValueError("groups must split E evenly into groups of at least 2")
+    gs = E // n_group
+    out = np.empty((T, n_group), dtype=np.float64)
+    for t in range(T):
+        for g in range(n_group):
+            vals = sorted(keys[t, g * gs:(g + 1) * gs], reverse=True)
+            out[t, g] = vals[0] + vals[1]
+    return out
+
+
+def topk_experts_biased(scores: np.ndarray, score_bias: Optional[np.ndarray], k: int,
+                        n_group: int = 1, topk_group: int = 1) -> np.ndarray:
+    """idx[t, :] = the k experts with the largest s + b among the kept groups.
+
+    Ties (of experts and of groups) go to the lower index, as in
+    ``topk_experts``; the chosen list is ordered by s + b descending.
+    """
+    scores = np.asarray(scores, dtype=np.float64)
+    T, E = scores.shape
+    keys = scores + (0.0 if score_bias is None else np.asarray(score_bias, np.float64)[None, :])
+    allowed = [list(range(E)) for _ in range(T)]
+    if n_group > 1:
+        if not (1 <= topk_group <= n_group):
+            raise ValueError("need 1 <= topk_group <= n_group")
+        gsc = group_scores(keys, n_group)
+        gs = E // n_group
+        for t in range(T):
+            kept = sorted(range(n_group), key=lambda g: (-gsc[t, g], g))[:topk_group]
+            allowed[t] = [e for e in range(E) if e // gs in kept]
+    idx = np.empty((T, k), dtype=np.int64)
+    for t in range(T):
+        if k > len(allowed[t]):
+            raise ValueError("k exceeds the experts of the kept groups")
+        order = sorted(allowed[t], key=lambda e: (-keys[t, e], e))
+        idx[t] = order[:k]
+    return idx
+
+
+def update_score_bias(score_bias: np.ndarray, load: np.ndarray, gamma: float) -> np.ndarray:
+    """One bias step after a batch: an expert above the mean load loses gamma,
+    one below it gains gamma ([moe10]: "超载的专家 b_i 减 γ，不足的加 γ");
+    an expert exactly at the mean is left unchanged."""
+    load = np.asarray(load, dtype=np.float64)
+    return np.asarray(score_bias, dtype=np.float64) - gamma * np.sign(load - np.mean(load))
+
+
 def mean_router_prob(scores: np.ndarray) -> np.ndarray:
     """P_e = (1/T) sum_t score[t,e], the batch-mean router probability that
     the load statistics use ([moe10] "辅助损失", definition of P_i)."""
@@ -218,12 +282,22 @@ def swiglu_ffn(x_rows: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray,
 # ---------------------------------------------------------------------------
 
 def route(z: np.ndarray, k: int, gate: str, renormalize: bool,
-          routed_scaling_factor: float, capacity: Optional[int]) -> Dict[str, np.ndarray]:
-    """Scores, top-k, weights, mean probability and dispatch from logits z."""
+          routed_scaling_factor: float, capacity: Optional[int],
+          score_bias: Optional[np.ndarray] = None, n_group: int = 1,
+          topk_group: int = 1) -> Dict[str, np.ndarray]:
+    """Scores, top-k, weights, mean probability and dispatch from logits z.
+
+    Without a score bias or groups the k largest logits are chosen; with
+    either, the k largest s + b among the kept groups (``topk_experts_biased``).
+    The weights always come from the raw scores.
+    """
     z = np.asarray(z, dtype=np.float64)
     E = z.shape[1]
     scores = gate_scores(z, gate)
-    idx = topk_experts(z, k)
+    if score_bias is None and n_group <= 1:
+        idx = topk_experts(z, k)
+    else:
+        idx = topk_experts_biased(scores, score_bias, k, n_group, topk_group)
     g = topk_weights(scores, idx, renormalize, routed_scaling_factor)
     out = {"logits": z, "scores": scores, "topk_idx": idx, "topk_w": g,
            "mean_prob": mean_router_prob(scores)}
@@ -244,7 +318,9 @@ def moe_layer_forward(x: np.ndarray, w_router: np.ndarray, experts,
                       router_bias: Optional[np.ndarray] = None,
                       shared=None,
                       tokens: Optional[Sequence[int]] = None,
-                      logits: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+                      logits: Optional[np.ndarray] = None,
+                      score_bias: Optional[np.ndarray] = None,
+                      n_group: int = 1, topk_group: int = 1) -> Dict[str, np.ndarray]:
     """Per-expert grouped formulation (the block sketch's loop over experts).
 
     ``experts[e]`` returns (w_gate_e, w_up_e, w_down_e) as float64 arrays and
@@ -257,7 +333,8 @@ def moe_layer_forward(x: np.ndarray, w_router: np.ndarray, experts,
     x = np.asarray(x, dtype=np.float64)
     T = x.shape[0]
     z = router_logits(x, w_router, router_bias) if logits is None else np.asarray(logits, np.float64)
-    r = route(z, k, gate, renormalize, routed_scaling_factor, capacity)
+    r = route(z, k, gate, renormalize, routed_scaling_factor, capacity, score_bias, n_group,
+              topk_group)
     toks = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     pos = {int(t): i for i, t in enumerate(toks)}
     y = np.zeros((len(toks), x.shape[1]), dtype=np.float64)

@@ -365,3 +365,92 @@ def test_dropped_assignment_contributes_zero_no_rerenorm():
     assert r["topk_idx"][2].tolist() == [0, 2]
     want = g[2, 1] * O.swiglu_ffn(x[2:3], *ex[2])[0]
     np.testing.assert_allclose(r["y"][2], want, rtol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# DeepSeek-V3 auxiliary-loss-free bias and group-limited selection
+# ([moe10] "DeepSeek-V3 的无辅助损失偏置")
+# ---------------------------------------------------------------------------
+
+def test_bias_update_printed_trace(golden):
+    fx = golden("moe10_bias_update_trace.json")
+    steps = fx["steps"]
+    for before, after in zip(steps[:-1], steps[1:]):
+        b = O.update_score_bias(np.array(before["bias"]), np.array(before["load"]), fx["gamma"])
+        np.testing.assert_allclose(b, after["bias"], rtol=0, atol=1e-12)
+
+
+def test_bias_trace_replayed_with_constructed_scores(golden):
+    # the page's three load vectors come out of ranking by s + b, with the
+    # bias stepped between batches (the scores are a constructed witness)
+    fx = golden("moe10_bias_update_trace.json")
+    s = np.array(fx["constructed_scores"])
+    b = np.zeros(fx["E"])
+    for step in fx["steps"]:
+        np.testing.assert_allclose(b, step["bias"], atol=1e-12)
+        idx = O.topk_experts_biased(s, b, fx["k"])
+        load = np.bincount(idx[:, 0], minlength=fx["E"])
+        np.testing.assert_array_equal(load, step["load"])
+        b = O.update_score_bias(b, load, fx["gamma"])
+
+
+def test_bias_at_mean_load_unchanged():
+    b = O.update_score_bias(np.array([0.1, -0.2, 0.3]), np.array([2, 2, 2]), 0.5)
+    np.testing.assert_array_equal(b, [0.1, -0.2, 0.3])
+
+
+def test_weights_use_raw_scores_not_biased_keys():
+    # a large bias pulls expert 3 into every token's choice; its weight is
+    # still its own raw score over the raw scores of the chosen pair
+    rng = np.random.default_rng(5)
+    s = O.sigmoid(rng.normal(size=(20, 6)))
+    bias = np.array([0, 0, 0, 10.0, 0, 0])
+    r = O.route(np.log(s / (1 - s)), 2, "sigmoid", True, 2.5, None, score_bias=bias)
+    assert np.all(r["topk_idx"][:, 0] == 3)
+    for t in range(20):
+        e0, e1 = r["topk_idx"][t]
+        np.testing.assert_allclose(r["topk_w"][t], 2.5 * np.array([s[t, e0], s[t, e1]]) /
+                                   (s[t, e0] + s[t, e1]), rtol=1e-12)
+
+
+def test_zero_bias_no_groups_equals_logit_topk():
+    rng = np.random.default_rng(6)
+    z = rng.normal(size=(50, 16))
+    a = O.topk_experts(z, 4)
+    b = O.topk_experts_biased(O.sigmoid(z), np.zeros(16), 4)
+    np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("E,n_group,topk_group,k", [(8, 4, 2, 3), (12, 3, 2, 4), (16, 8, 4, 8),
+                                                    (6, 2, 1, 2)])
+def test_group_limited_selection_brute_force(E, n_group, topk_group, k):
+    # independent formulation: a group's score is the best pair sum inside it;
+    # the kept groups are the topk_group-subset with the largest total; the
+    # chosen experts are the k-subset of their experts with the largest total
+    rng = np.random.default_rng(E * 100 + k)
+    s = rng.uniform(size=(30, E))
+    bias = rng.normal(scale=0.1, size=E)
+    keys = s + bias[None, :]
+    gs = E // n_group
+    idx = O.topk_experts_biased(s, bias, k, n_group, topk_group)
+    gsc = O.group_scores(keys, n_group)
+    for t in range(30):
+        for g in range(n_group):
+            members = range(g * gs, (g + 1) * gs)
+            best = max(keys[t, i] + keys[t, j] for i, j in itertools.combinations(members, 2))
+            assert gsc[t, g] == pytest.approx(best, abs=1e-15)
+        kept = max(itertools.combinations(range(n_group), topk_group),
+                   key=lambda c: sum(gsc[t, g] for g in c))
+        pool = [e for e in range(E) if e // gs in kept]
+        chosen = max(itertools.combinations(pool, k), key=lambda c: sum(keys[t, e] for e in c))
+        assert sorted(idx[t]) == sorted(chosen)
+        assert all(keys[t, idx[t, j]] >= keys[t, idx[t, j + 1]] for j in range(k - 1))
+
+
+def test_deepseek_v3_groups_limit_each_token_to_four_groups():
+    # 256 experts in 8 groups of 32, 4 groups kept, top-8: every token's
+    # experts lie in at most 4 groups ([routing]: at most 4 nodes per token)
+    rng = np.random.default_rng(7)
+    s = O.sigmoid(rng.normal(size=(40, 256)))
+    idx = O.topk_experts_biased(s, rng.normal(scale=0.01, size=256), 8, 8, 4)
+    assert all(len(set(int(e) // 32 for e in row)) <= 4 for row in idx)
