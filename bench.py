@@ -41,6 +41,9 @@ WORKLOAD_TEXT = {
                     "d_ff=2048, 1 shared expert d_ff=2048, sigmoid, renorm x2.5, bf16)",
     "switch": "Switch-style capacity layer (T=16384, d=2048, E=64 top-1, d_ff=8192, softmax, "
               "C=ceil(T/E*1.25)=320, Zipf(1.2) router bias, bf16)",
+    "dsv3_prefill_noaux": "DeepSeek-V3-shaped MoE prefill layer with DeepSeek-V3's router "
+                          "(T=8192, d=7168, E=256 top-8 ranked by sigmoid + selection bias, "
+                          "8 groups / 4 kept, d_ff=2048, 1 shared expert, renorm x2.5, bf16)",
     "dsv3_decode": "DeepSeek-V3-shaped decode layer (T=64, d=7168, E=256 top-8, d_ff=2048, "
                    "1 shared expert, sigmoid, renorm x2.5, bf16)",
     "tiny": "tiny fp32 layer (T=64, d=128, E=4 top-2, d_ff=256)",
@@ -216,7 +219,9 @@ def time_oracle(shape, inputs, sample_tokens: int, steps: int, warmup: int = 0):
         t0 = time.perf_counter()
         O.moe_layer_forward(x, wr, experts, k=shape.k, gate=shape.gate,
                             renormalize=shape.renormalize, routed_scaling_factor=shape.rsf,
-                            capacity=cap, router_bias=bias, shared=shared, tokens=toks)
+                            capacity=cap, router_bias=bias, shared=shared, tokens=toks,
+                            score_bias=to_f64(inputs.get("score_bias")),
+                            n_group=max(shape.n_group, 1), topk_group=shape.topk_group)
         if i >= warmup:
             times.append(time.perf_counter() - t0)
     return times
@@ -325,10 +330,10 @@ def main(argv=None):
     warm_events = new_events(NS + 1)
 
     def step(evs):
-        return moe.moe_layer_forward_profiled(cfg, x, w.w_router, w.router_bias, w.w_gate,
-                                              w.w_up, w.w_down, w.ws_gate, w.ws_up, w.ws_down,
-                                              y, topk_idx, topk_w, counts, drops, mean_prob,
-                                              ws, evs, stream)
+        return moe.moe_layer_forward_profiled(cfg, x, w.w_router, w.router_bias, w.score_bias,
+                                              w.w_gate, w.w_up, w.w_down, w.ws_gate, w.ws_up,
+                                              w.ws_down, y, topk_idx, topk_w, counts, drops,
+                                              mean_prob, ws, evs, stream)
 
     for _ in range(args.warmup):
         step(warm_events)

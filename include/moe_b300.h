@@ -87,6 +87,10 @@ typedef struct {
   int32_t capacity;       /* < 0: unlimited; >= 0: kept slots per expert (0 drops all) */
   int32_t act_dtype;      /* moe_dtype_t of x, weights and the expert activations */
   int32_t out_dtype;      /* moe_dtype_t of y                                   */
+  int32_t n_group;        /* expert groups for group-limited selection; 0 or 1 = none.
+                             Otherwise 2..32, dividing n_experts into groups of >= 2 */
+  int32_t topk_group;     /* groups kept per token when n_group > 1 (1..n_group;
+                             top_k <= topk_group * n_experts / n_group)           */
 } moe_config_t;
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
@@ -108,10 +112,26 @@ MOE_API moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
 MOE_API moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_bytes,
                                 void* stream);
 
+/* Selection rule shared by moe_router_topk, moe_topk_from_logits and the
+ * layer forward.  Scores are s = softmax(z) or sigmoid(z) of the fp32 logits.
+ *   - score_bias == NULL and n_group <= 1: the k largest LOGITS are chosen
+ *     (the same experts as the k largest scores), ties to the lower index.
+ *   - otherwise (DeepSeek-V3 auxiliary-loss-free routing, "10. 混合专家 MoE",
+ *     section "DeepSeek-V3 的无辅助损失偏置"): the ranking key is
+ *     s_e + score_bias[e] (fp32; bias 0 when NULL).  With n_group > 1 the
+ *     experts form n_group consecutive groups of E / n_group, a group's score
+ *     is the sum of its two largest keys, the topk_group best groups are kept
+ *     (ties to the lower group) and the k largest keys among their experts
+ *     are chosen (ties to the lower index).  The combine weights use the raw
+ *     scores s, never the bias.
+ * topk_idx lists the chosen experts by ranking key, descending. */
+
 /* Router + gating + top-k (the block sketch's first four lines).
  *   x [T, d] act_dtype; w_router [E, d] act_dtype;
  *   router_bias [E] fp32 or NULL: added to every logit before scoring and
  *     selection (used by the Zipf-skewed Switch-style layer);
+ *   score_bias [E] fp32 or NULL: selection-only bias on the scores (see the
+ *     selection rule above; DeepSeek-V3's e_score_correction_bias);
  *   logits_out [T, E] fp32 or NULL: the logits incl. bias;
  *   topk_idx [T, k] int32: chosen experts, logit descending, ties to the
  *     lower expert index;
@@ -119,16 +139,33 @@ MOE_API moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_
  *   mean_prob [E] fp32 or NULL: (1/T) sum_t score[t, e] over ALL experts
  *     (softmax probability or sigmoid score), reduced in a fixed order. */
 MOE_API moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x, const void* w_router,
-                             const float* router_bias, float* logits_out,
+                             const float* router_bias, const float* score_bias,
+                             float* logits_out,
                              int32_t* topk_idx, float* topk_w, float* mean_prob,
                              void* ws, size_t ws_bytes, void* stream);
 
-/* Gating + top-k from caller-supplied fp32 logits [T, E] (bias already in).
- * Outputs as moe_router_topk.  The selection compares fp32 logits only, so
- * it is reproducible bit for bit from the same logits. */
+/* Gating + top-k from caller-supplied fp32 logits [T, E] (router bias
+ * already in), with the optional selection-only score_bias [E].  Outputs as
+ * moe_router_topk.  Without score bias or groups the selection compares fp32
+ * logits only, so it is reproducible bit for bit from the same logits; with
+ * them it compares fp32 s + b, which depends on the fp32 exp. */
 MOE_API moe_status_t moe_topk_from_logits(const moe_config_t* cfg, const float* logits,
+                                  const float* score_bias,
                                   int32_t* topk_idx, float* topk_w, float* mean_prob,
                                   void* ws, size_t ws_bytes, void* stream);
+
+/* One step of the auxiliary-loss-free bias ("DeepSeek-V3 的无辅助损失偏置":
+ * after each batch an overloaded expert's bias is lowered by gamma and an
+ * underloaded one's raised by gamma):
+ *   load[e] = counts[e] + drops[e]  (drops may be NULL),
+ *   score_bias[e] -= gamma * sign(E * load[e] - sum_e' load[e'])
+ * i.e. compared with the mean load exactly, in integers; an expert exactly
+ * at the mean keeps its bias.  counts, drops: [E] int32 device (as written
+ * by moe_dispatch or the layer forward); score_bias: [E] fp32 device,
+ * updated in place.  One small kernel on `stream`. */
+MOE_API moe_status_t moe_update_score_bias(const moe_config_t* cfg, const int32_t* counts,
+                                           const int32_t* drops, float gamma, float* score_bias,
+                                           void* stream);
 
 /* Capacity + dispatch ("负载不均：路由坍缩与丢 token"; the block sketch's
  * per-expert grouping).  Assignments are visited in ascending a; each takes
@@ -203,11 +240,11 @@ MOE_API moe_status_t moe_combine(const moe_config_t* cfg, const float* y_perm, c
  * router -> gating/top-k -> capacity/dispatch -> gather -> grouped gate/up +
  * SwiGLU -> grouped down -> combine.
  *   y [T, d] out_dtype (required);
- *   router_bias, ws_gate/ws_up/ws_down (all or none) may be NULL;
+ *   router_bias, score_bias, ws_gate/ws_up/ws_down (all or none) may be NULL;
  *   topk_idx [T, k], topk_w [T, k], counts [E], drops [E], mean_prob [E]
  *     are optional outputs (NULL = not returned). */
 MOE_API moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const void* w_router,
-                               const float* router_bias,
+                               const float* router_bias, const float* score_bias,
                                const void* w_gate, const void* w_up, const void* w_down,
                                const void* ws_gate, const void* ws_up, const void* ws_down,
                                void* y, int32_t* topk_idx, float* topk_w,
@@ -234,7 +271,7 @@ typedef enum {
  * moe_layer_forward. */
 MOE_API moe_status_t moe_layer_forward_profiled(
     const moe_config_t* cfg, const void* x, const void* w_router, const float* router_bias,
-    const void* w_gate, const void* w_up, const void* w_down, const void* ws_gate,
+    const float* score_bias, const void* w_gate, const void* w_up, const void* w_down, const void* ws_gate,
     const void* ws_up, const void* ws_down, void* y, int32_t* topk_idx, float* topk_w,
     int32_t* counts, int32_t* drops, float* mean_prob, void* ws, size_t ws_bytes, void* stream,
     void** stage_events, int32_t* n_launches);

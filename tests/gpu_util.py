@@ -79,7 +79,35 @@ def oracle_layer(shape, inputs, tokens: Optional[Sequence[int]] = None):
         k=shape.k, gate=shape.gate, renormalize=shape.renormalize,
         routed_scaling_factor=shape.rsf, capacity=oracle_capacity(shape, T),
         router_bias=to_f64(inputs["router_bias"]), shared=shared_weights(inputs),
-        tokens=tokens)
+        tokens=tokens, score_bias=to_f64(inputs.get("score_bias")),
+        n_group=max(shape.n_group, 1), topk_group=shape.topk_group)
+
+
+def biased_margins(scores: np.ndarray, bias: Optional[np.ndarray], idx: np.ndarray,
+                   n_group: int, topk_group: int) -> np.ndarray:
+    """Per token, for selection by s + b among kept groups: the smaller of
+    (k-th chosen key - best unchosen key of the kept groups) and, with groups,
+    (last kept group score - best dropped group score).  Decisions within
+    this margin depend on the rounding of s + b."""
+    T, k = idx.shape
+    E = scores.shape[1]
+    keys = scores + (0.0 if bias is None else bias[None, :])
+    m = np.full(T, np.inf)
+    if n_group > 1:
+        gsc = O.group_scores(keys, n_group)
+        gs = E // n_group
+    for t in range(T):
+        allowed = np.ones(E, dtype=bool)
+        if n_group > 1:
+            order = sorted(range(n_group), key=lambda g: (-gsc[t, g], g))
+            kept = order[:topk_group]
+            if topk_group < n_group:
+                m[t] = gsc[t, kept[-1]] - gsc[t, order[topk_group]]
+            allowed = np.array([e // gs in kept for e in range(E)])
+        rest = [keys[t, e] for e in range(E) if allowed[e] and e not in set(idx[t].tolist())]
+        if rest:
+            m[t] = min(m[t], keys[t, idx[t, k - 1]] - max(rest))
+    return m
 
 
 def np_i(t: torch.Tensor) -> np.ndarray:

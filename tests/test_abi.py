@@ -115,36 +115,65 @@ def test_entry_points_reject_missing_workspace_and_pointers():
     _, need = _ws_size(cfg)
     fake = 0x10000   # never dereferenced: validation fails before any launch
     # workspace too small / misaligned / null
-    assert lib.moe_topk_from_logits(ctypes.byref(cfg), fake, fake, fake, None, fake, need - 1,
+    assert lib.moe_topk_from_logits(ctypes.byref(cfg), fake, None, fake, fake, None, fake, need - 1,
                                     None) == B.MOE_ERR_WORKSPACE
-    assert lib.moe_topk_from_logits(ctypes.byref(cfg), fake, fake, fake, None, fake + 16, need,
+    assert lib.moe_topk_from_logits(ctypes.byref(cfg), fake, None, fake, fake, None, fake + 16, need,
                                     None) == B.MOE_ERR_WORKSPACE
-    assert lib.moe_topk_from_logits(ctypes.byref(cfg), fake, fake, fake, None, None, need,
+    assert lib.moe_topk_from_logits(ctypes.byref(cfg), fake, None, fake, fake, None, None, need,
                                     None) == B.MOE_ERR_WORKSPACE
     # null required pointer
-    assert lib.moe_topk_from_logits(ctypes.byref(cfg), None, fake, fake, None, fake, need,
+    assert lib.moe_topk_from_logits(ctypes.byref(cfg), None, None, fake, fake, None, fake, need,
                                     None) == B.MOE_ERR_INVALID_ARG
     # misaligned logits
-    assert lib.moe_topk_from_logits(ctypes.byref(cfg), fake + 4, fake, fake, None, fake, need,
+    assert lib.moe_topk_from_logits(ctypes.byref(cfg), fake + 4, None, fake, fake, None, fake, need,
                                     None) == B.MOE_ERR_INVALID_ARG
     # dispatch: null counts
     assert lib.moe_dispatch(ctypes.byref(cfg), fake, None, fake, fake, fake, fake, fake, need,
                             None) == B.MOE_ERR_INVALID_ARG
     # layer: shared weights given although d_ff_shared == 0
-    assert lib.moe_layer_forward(ctypes.byref(cfg), fake, fake, None, fake, fake, fake, fake,
+    assert lib.moe_layer_forward(ctypes.byref(cfg), fake, fake, None, None, fake, fake, fake, fake,
                                  fake, fake, fake, None, None, None, None, None, fake, need,
                                  None) == B.MOE_ERR_INVALID_ARG
     # layer: only some shared weights
     cs = _cfg(F_s=128)
     _, need_s = _ws_size(cs)
-    assert lib.moe_layer_forward(ctypes.byref(cs), fake, fake, None, fake, fake, fake, fake,
+    assert lib.moe_layer_forward(ctypes.byref(cs), fake, fake, None, None, fake, fake, fake, fake,
                                  None, fake, fake, None, None, None, None, None, fake, need_s,
                                  None) == B.MOE_ERR_INVALID_ARG
     # null config
-    assert lib.moe_layer_forward(None, fake, fake, None, fake, fake, fake, None, None, None,
+    assert lib.moe_layer_forward(None, fake, fake, None, None, fake, fake, fake, None, None, None,
                                  fake, None, None, None, None, None, fake, need,
                                  None) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_get_error(None, None) == B.MOE_ERR_WORKSPACE
+    # misaligned selection bias
+    assert lib.moe_topk_from_logits(ctypes.byref(cfg), fake, fake + 4, fake, fake, None, fake,
+                                    need, None) == B.MOE_ERR_INVALID_ARG
+    # score-bias step: null counts / bias, non-finite gamma
+    assert lib.moe_update_score_bias(ctypes.byref(cfg), None, None, 0.001, fake,
+                                     None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_update_score_bias(ctypes.byref(cfg), fake, None, 0.001, None,
+                                     None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_update_score_bias(ctypes.byref(cfg), fake, None, float("nan"), fake,
+                                     None) == B.MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("E,k,n_group,topk_group,want", [
+    (256, 8, 8, 4, B.MOE_OK),               # DeepSeek-V3: 8 groups of 32, keep 4
+    (16, 2, 0, 0, B.MOE_OK),                # no groups
+    (16, 2, 1, 0, B.MOE_OK),                # one group = no groups
+    (16, 2, 3, 1, B.MOE_ERR_INVALID_ARG),   # 3 does not divide 16
+    (16, 2, 16, 4, B.MOE_ERR_INVALID_ARG),  # groups of one expert
+    (16, 2, 4, 0, B.MOE_ERR_INVALID_ARG),   # no group kept
+    (16, 2, 4, 5, B.MOE_ERR_INVALID_ARG),   # more groups kept than exist
+    (16, 9, 4, 2, B.MOE_ERR_INVALID_ARG),   # k larger than the kept experts (8)
+    (128, 2, 64, 4, B.MOE_ERR_UNSUPPORTED), # more than 32 groups
+    (16, 2, -1, 0, B.MOE_ERR_INVALID_ARG),
+])
+def test_group_fields_validated(E, k, n_group, topk_group, want):
+    c = _cfg(E=E, k=k)
+    c.n_group = n_group
+    c.topk_group = topk_group
+    assert _ws_size(c)[0] == want
 
 
 def test_config_from_shape_capacity():

@@ -8,6 +8,6 @@ from ._binding import MoEConfig, MoEError, load_library  # noqa: F401
 from .api import (  # noqa: F401
     LayerWeights, Workspace, config_from_shape, dispatch, layer_forward, make_config,
     moe_capacity, moe_combine, moe_dispatch, moe_get_error, moe_grouped_swiglu,
-    moe_layer_forward, moe_layer_forward_profiled, moe_router_topk, moe_topk_from_logits, moe_version,
-    moe_workspace_size, route, topk_from_logits,
+    moe_layer_forward, moe_layer_forward_profiled, moe_router_topk, moe_topk_from_logits,
+    moe_update_score_bias, moe_version, moe_workspace_size, route, topk_from_logits,
 )

@@ -45,6 +45,8 @@ class MoEConfig(ctypes.Structure):
         ("capacity", c_int32),
         ("act_dtype", c_int32),
         ("out_dtype", c_int32),
+        ("n_group", c_int32),
+        ("topk_group", c_int32),
     ]
 
     def __repr__(self):
@@ -62,9 +64,10 @@ SIGNATURES = {
     "moe_workspace_size": (c_int32, [CFG, POINTER(c_size_t)]),
     "moe_workspace_init": (c_int32, [CFG, c_void_p, c_size_t, c_void_p]),
     "moe_router_topk": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                  c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
-    "moe_topk_from_logits": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p,
+                                  c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "moe_topk_from_logits": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                        c_void_p, c_size_t, c_void_p]),
+    "moe_update_score_bias": (c_int32, [CFG, c_void_p, c_void_p, c_float, c_void_p, c_void_p]),
     "moe_dispatch": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_dispatch_no_workspace": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -77,12 +80,12 @@ SIGNATURES = {
     "moe_layer_forward": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                    c_void_p, c_size_t, c_void_p]),
+                                    c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_layer_forward_profiled": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p,
                                              c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                              c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                             c_void_p, c_void_p, c_size_t, c_void_p, c_void_p,
-                                             c_void_p]),
+                                             c_void_p, c_void_p, c_void_p, c_size_t, c_void_p,
+                                             c_void_p, c_void_p]),
     "moe_get_error": (c_int32, [c_void_p, c_void_p]),
     "moe_selftest_bounded_wait": (c_int32, [c_void_p, c_size_t, ctypes.c_uint64, c_void_p]),
 }

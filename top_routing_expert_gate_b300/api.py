@@ -24,11 +24,13 @@ _TORCH_DT = {B.MOE_BF16: torch.bfloat16, B.MOE_FP32: torch.float32}
 
 def make_config(T: int, d: int, E: int, k: int, F: int, F_s: int = 0, gate: str = "softmax",
                 renormalize: bool = True, rsf: float = 1.0, capacity: int = -1,
-                act_dtype: str = "bf16", out_dtype: str = "fp32") -> MoEConfig:
+                act_dtype: str = "bf16", out_dtype: str = "fp32", n_group: int = 0,
+                topk_group: int = 0) -> MoEConfig:
     return MoEConfig(T=T, d_model=d, n_experts=E, top_k=k, d_ff=F, d_ff_shared=F_s,
                      gate=B.MOE_GATE_SOFTMAX if gate == "softmax" else B.MOE_GATE_SIGMOID,
                      renormalize=1 if renormalize else 0, routed_scaling_factor=float(rsf),
-                     capacity=int(capacity), act_dtype=_DT[act_dtype], out_dtype=_DT[out_dtype])
+                     capacity=int(capacity), act_dtype=_DT[act_dtype], out_dtype=_DT[out_dtype],
+                     n_group=int(n_group), topk_group=int(topk_group))
 
 
 def config_from_shape(shape, out_dtype: str = "fp32", T: Optional[int] = None) -> MoEConfig:
@@ -38,7 +40,8 @@ def config_from_shape(shape, out_dtype: str = "fp32", T: Optional[int] = None) -
     if shape.capacity_factor is not None:
         cap = moe_capacity(T, shape.E, shape.capacity_factor)
     return make_config(T, shape.d, shape.E, shape.k, shape.F, shape.F_s, shape.gate,
-                       shape.renormalize, shape.rsf, cap, shape.dtype, out_dtype)
+                       shape.renormalize, shape.rsf, cap, shape.dtype, out_dtype,
+                       getattr(shape, "n_group", 0), getattr(shape, "topk_group", 0))
 
 
 def act_dtype(cfg: MoEConfig) -> torch.dtype:
@@ -98,19 +101,26 @@ class Workspace:
                                                 _stream(None)), "moe_workspace_init")
 
 
-def moe_router_topk(cfg, x, w_router, router_bias, logits_out, topk_idx, topk_w, mean_prob,
-                    ws: Workspace, stream=None) -> None:
+def moe_router_topk(cfg, x, w_router, router_bias, score_bias, logits_out, topk_idx, topk_w,
+                    mean_prob, ws: Workspace, stream=None) -> None:
     check(load_library().moe_router_topk(
         ctypes.byref(cfg), _ptr(x, "x"), _ptr(w_router, "w_router"), _ptr(router_bias),
-        _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), _ptr(mean_prob), ws.ptr, ws.nbytes,
-        _stream(stream)), "moe_router_topk")
+        _ptr(score_bias), _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), _ptr(mean_prob),
+        ws.ptr, ws.nbytes, _stream(stream)), "moe_router_topk")
 
 
-def moe_topk_from_logits(cfg, logits, topk_idx, topk_w, mean_prob, ws: Workspace,
+def moe_topk_from_logits(cfg, logits, score_bias, topk_idx, topk_w, mean_prob, ws: Workspace,
                          stream=None) -> None:
     check(load_library().moe_topk_from_logits(
-        ctypes.byref(cfg), _ptr(logits, "logits"), _ptr(topk_idx), _ptr(topk_w),
-        _ptr(mean_prob), ws.ptr, ws.nbytes, _stream(stream)), "moe_topk_from_logits")
+        ctypes.byref(cfg), _ptr(logits, "logits"), _ptr(score_bias), _ptr(topk_idx),
+        _ptr(topk_w), _ptr(mean_prob), ws.ptr, ws.nbytes, _stream(stream)),
+        "moe_topk_from_logits")
+
+
+def moe_update_score_bias(cfg, counts, drops, gamma: float, score_bias, stream=None) -> None:
+    check(load_library().moe_update_score_bias(
+        ctypes.byref(cfg), _ptr(counts, "counts"), _ptr(drops), float(gamma),
+        _ptr(score_bias, "score_bias"), _stream(stream)), "moe_update_score_bias")
 
 
 def moe_dispatch(cfg, topk_idx, counts, drops, offsets, perm, drop_mask, ws: Workspace,
@@ -136,19 +146,20 @@ def moe_combine(cfg, y_perm, topk_w, offsets, perm, drop_mask, y_shared, y, ws: 
         "moe_combine")
 
 
-def moe_layer_forward(cfg, x, w_router, router_bias, w_gate, w_up, w_down, ws_gate, ws_up,
-                      ws_down, y, topk_idx, topk_w, counts, drops, mean_prob, ws: Workspace,
-                      stream=None) -> None:
+def moe_layer_forward(cfg, x, w_router, router_bias, score_bias, w_gate, w_up, w_down, ws_gate,
+                      ws_up, ws_down, y, topk_idx, topk_w, counts, drops, mean_prob,
+                      ws: Workspace, stream=None) -> None:
     check(load_library().moe_layer_forward(
-        ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(w_gate),
+        ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(score_bias),
+        _ptr(w_gate),
         _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), _ptr(y),
         _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(drops), _ptr(mean_prob), ws.ptr,
         ws.nbytes, _stream(stream)), "moe_layer_forward")
 
 
-def moe_layer_forward_profiled(cfg, x, w_router, router_bias, w_gate, w_up, w_down, ws_gate,
-                               ws_up, ws_down, y, topk_idx, topk_w, counts, drops, mean_prob,
-                               ws: Workspace, stage_events, stream=None) -> int:
+def moe_layer_forward_profiled(cfg, x, w_router, router_bias, score_bias, w_gate, w_up, w_down,
+                               ws_gate, ws_up, ws_down, y, topk_idx, topk_w, counts, drops,
+                               mean_prob, ws: Workspace, stage_events, stream=None) -> int:
     """moe_layer_forward recording ``stage_events`` (MOE_NUM_STAGES + 1
     torch.cuda.Event with timing, already recorded once so that they exist)
     before each stage; returns the number of kernels the call launched."""
@@ -157,7 +168,8 @@ def moe_layer_forward_profiled(cfg, x, w_router, router_bias, w_gate, w_up, w_do
     arr = (ctypes.c_void_p * len(stage_events))(*[e.cuda_event for e in stage_events])
     n = ctypes.c_int32(0)
     check(load_library().moe_layer_forward_profiled(
-        ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(w_gate),
+        ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(score_bias),
+        _ptr(w_gate),
         _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), _ptr(y),
         _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(drops), _ptr(mean_prob), ws.ptr,
         ws.nbytes, _stream(stream), arr, ctypes.byref(n)), "moe_layer_forward_profiled")
@@ -182,25 +194,27 @@ def _f32(n, device):
 
 
 def route(cfg, x, w_router, router_bias=None, ws: Optional[Workspace] = None,
-          want_logits=True) -> Dict[str, torch.Tensor]:
+          want_logits=True, score_bias=None) -> Dict[str, torch.Tensor]:
     dev = x.device
     ws = ws or Workspace(cfg, dev)
     T, E, k = cfg.T, cfg.n_experts, cfg.top_k
     out = {"topk_idx": _i32((T, k), dev), "topk_w": _f32((T, k), dev),
            "mean_prob": _f32(E, dev)}
     out["logits"] = _f32((T, E), dev) if want_logits else None
-    moe_router_topk(cfg, x, w_router, router_bias, out["logits"], out["topk_idx"],
+    moe_router_topk(cfg, x, w_router, router_bias, score_bias, out["logits"], out["topk_idx"],
                     out["topk_w"], out["mean_prob"], ws)
     return out
 
 
-def topk_from_logits(cfg, logits, ws: Optional[Workspace] = None) -> Dict[str, torch.Tensor]:
+def topk_from_logits(cfg, logits, ws: Optional[Workspace] = None,
+                     score_bias=None) -> Dict[str, torch.Tensor]:
     dev = logits.device
     ws = ws or Workspace(cfg, dev)
     T, E, k = cfg.T, cfg.n_experts, cfg.top_k
     out = {"topk_idx": _i32((T, k), dev), "topk_w": _f32((T, k), dev),
            "mean_prob": _f32(E, dev)}
-    moe_topk_from_logits(cfg, logits, out["topk_idx"], out["topk_w"], out["mean_prob"], ws)
+    moe_topk_from_logits(cfg, logits, score_bias, out["topk_idx"], out["topk_w"],
+                         out["mean_prob"], ws)
     return out
 
 
@@ -226,12 +240,13 @@ class LayerWeights:
     ws_gate: Optional[torch.Tensor] = None
     ws_up: Optional[torch.Tensor] = None
     ws_down: Optional[torch.Tensor] = None
+    score_bias: Optional[torch.Tensor] = None
 
     @classmethod
     def from_inputs(cls, inputs) -> "LayerWeights":
         return cls(inputs["w_router"], inputs["w_gate"], inputs["w_up"], inputs["w_down"],
                    inputs.get("router_bias"), inputs.get("ws_gate"), inputs.get("ws_up"),
-                   inputs.get("ws_down"))
+                   inputs.get("ws_down"), inputs.get("score_bias"))
 
 
 def layer_forward(cfg, x, w: LayerWeights, ws: Optional[Workspace] = None,
@@ -245,7 +260,7 @@ def layer_forward(cfg, x, w: LayerWeights, ws: Optional[Workspace] = None,
         out.update(topk_idx=_i32((T, k), dev), topk_w=_f32((T, k), dev), counts=_i32(E, dev),
                    drops=_i32(E, dev), mean_prob=_f32(E, dev))
     g = out.get
-    moe_layer_forward(cfg, x, w.w_router, w.router_bias, w.w_gate, w.w_up, w.w_down, w.ws_gate,
-                      w.ws_up, w.ws_down, out["y"], g("topk_idx"), g("topk_w"), g("counts"),
-                      g("drops"), g("mean_prob"), ws, stream)
+    moe_layer_forward(cfg, x, w.w_router, w.router_bias, w.score_bias, w.w_gate, w.w_up,
+                      w.w_down, w.ws_gate, w.ws_up, w.ws_down, out["y"], g("topk_idx"),
+                      g("topk_w"), g("counts"), g("drops"), g("mean_prob"), ws, stream)
     return out

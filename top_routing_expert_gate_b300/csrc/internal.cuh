@@ -105,9 +105,16 @@ cudaError_t launch_router_tc(const moe_config_t& c, const void* x, const void* w
 // Gating + top-k from logits; writes the summed logits to logits_out when
 // given; mp_partial receives per-block partial sums of the scores, then a
 // finalize kernel writes mean_prob (may be null).
-cudaError_t launch_topk(const moe_config_t& c, const LogitsView& z, float* logits_out,
-                        int32_t* idx, float* w, float* mp_partial, float* mean_prob,
-                        cudaStream_t s, LaunchCounter* lc = nullptr);
+// score_bias (nullable) and cfg.n_group / topk_group switch the ranking to
+// s + b with group-limited selection (include/moe_b300.h, selection rule).
+cudaError_t launch_topk(const moe_config_t& c, const LogitsView& z, const float* score_bias,
+                        float* logits_out, int32_t* idx, float* w, float* mp_partial,
+                        float* mean_prob, cudaStream_t s, LaunchCounter* lc = nullptr);
+
+// b_e -= gamma * sign(E * load_e - sum load), load = counts (+ drops).
+cudaError_t launch_score_bias_update(const moe_config_t& c, const int32_t* counts,
+                                     const int32_t* drops, float gamma, float* bias,
+                                     cudaStream_t s);
 
 // Dispatch: histogram, scan, stable scatter.  row_of may be null.
 cudaError_t launch_dispatch(const moe_config_t& c, const int32_t* idx, int32_t* block_hist,

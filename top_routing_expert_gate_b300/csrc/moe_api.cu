@@ -78,6 +78,17 @@ moe_status_t check_config(const moe_config_t* c) {
     if (c->d_model % 64 != 0 || c->d_ff % 128 != 0 || c->d_ff_shared % 128 != 0)
       return MOE_ERR_UNSUPPORTED;
   }
+  // expert groups: 0 or 1 = none; otherwise equal groups of at least two
+  // experts, at most 32 groups (one warp lane scores each group)
+  if (c->n_group < 0) return MOE_ERR_INVALID_ARG;
+  if (c->n_group > 1) {
+    if (c->n_experts % c->n_group != 0 || c->n_experts / c->n_group < 2)
+      return MOE_ERR_INVALID_ARG;
+    if (c->n_group > 32) return MOE_ERR_UNSUPPORTED;
+    if (c->topk_group < 1 || c->topk_group > c->n_group) return MOE_ERR_INVALID_ARG;
+    if ((long long)c->top_k > (long long)c->topk_group * (c->n_experts / c->n_group))
+      return MOE_ERR_INVALID_ARG;
+  }
   return MOE_OK;
 }
 
@@ -153,7 +164,7 @@ moe_status_t check_shared_args(const moe_config_t* c, const void* g, const void*
 
 extern "C" {
 
-int32_t moe_version(void) { return 100; }
+int32_t moe_version(void) { return 200; }
 
 const char* moe_status_string(moe_status_t st) {
   switch (st) {
@@ -191,27 +202,39 @@ moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_byt
 }
 
 moe_status_t moe_topk_from_logits(const moe_config_t* cfg, const float* logits,
-                                  int32_t* topk_idx, float* topk_w, float* mean_prob,
-                                  void* ws, size_t ws_bytes, void* stream) {
+                                  const float* score_bias, int32_t* topk_idx, float* topk_w,
+                                  float* mean_prob, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(check_config(cfg));
   MOE_TRY(check_ws(cfg, ws, ws_bytes));
   if (bad_ptr(cfg, logits) || bad_ptr(cfg, topk_idx) || bad_ptr(cfg, topk_w) ||
-      bad_opt(mean_prob))
+      bad_opt(mean_prob) || bad_opt(score_bias))
     return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(*cfg);
   const LogitsView view{logits, 1, 0, nullptr};
-  return cuda_status(launch_topk(*cfg, view, nullptr, topk_idx, topk_w,
+  return cuda_status(launch_topk(*cfg, view, score_bias, nullptr, topk_idx, topk_w,
                                  at<float>(ws, L.mp_partial), mean_prob, (cudaStream_t)stream));
 }
 
+moe_status_t moe_update_score_bias(const moe_config_t* cfg, const int32_t* counts,
+                                   const int32_t* drops, float gamma, float* score_bias,
+                                   void* stream) {
+  MOE_TRY(check_config(cfg));
+  if (!counts || !score_bias || !aligned16(counts) || !aligned16(score_bias) || bad_opt(drops))
+    return MOE_ERR_INVALID_ARG;
+  if (!isfinite(gamma)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_score_bias_update(*cfg, counts, drops, gamma, score_bias, (cudaStream_t)stream));
+}
+
 moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x, const void* w_router,
-                             const float* router_bias, float* logits_out, int32_t* topk_idx,
-                             float* topk_w, float* mean_prob, void* ws, size_t ws_bytes,
-                             void* stream) {
+                             const float* router_bias, const float* score_bias,
+                             float* logits_out, int32_t* topk_idx, float* topk_w,
+                             float* mean_prob, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(check_config(cfg));
   MOE_TRY(check_ws(cfg, ws, ws_bytes));
   if (bad_ptr(cfg, x) || bad_ptr(cfg, w_router) || bad_ptr(cfg, topk_idx) ||
-      bad_ptr(cfg, topk_w) || bad_opt(router_bias) || bad_opt(logits_out) || bad_opt(mean_prob))
+      bad_ptr(cfg, topk_w) || bad_opt(router_bias) || bad_opt(score_bias) ||
+      bad_opt(logits_out) || bad_opt(mean_prob))
     return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(*cfg);
   cudaStream_t s = (cudaStream_t)stream;
@@ -219,7 +242,7 @@ moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x, const void*
   LogitsView view{};
   MOE_TRY_CUDA(launch_router(*cfg, x, w_router, router_bias, at<float>(ws, L.logits), &view,
                              status, s));
-  return cuda_status(launch_topk(*cfg, view, logits_out, topk_idx, topk_w,
+  return cuda_status(launch_topk(*cfg, view, score_bias, logits_out, topk_idx, topk_w,
                                  at<float>(ws, L.mp_partial), mean_prob, s));
 }
 
@@ -302,7 +325,8 @@ namespace {
 // The layer forward.  When `ev` is non-null, ev[i] is recorded on the stream
 // before stage i (MOE_NUM_STAGES stages) and ev[MOE_NUM_STAGES] after the last.
 moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const void* w_router,
-                                const float* router_bias, const void* w_gate, const void* w_up,
+                                const float* router_bias, const float* score_bias,
+                                const void* w_gate, const void* w_up,
                                 const void* w_down, const void* ws_gate, const void* ws_up,
                                 const void* ws_down, void* y, int32_t* topk_idx, float* topk_w,
                                 int32_t* counts, int32_t* drops, float* mean_prob, void* ws,
@@ -312,6 +336,7 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
   MOE_TRY(check_ws(cfg, ws, ws_bytes));
   if (bad_ptr(cfg, x) || bad_ptr(cfg, w_router) || bad_ptr(cfg, w_gate) ||
       bad_ptr(cfg, w_up) || bad_ptr(cfg, w_down) || bad_ptr(cfg, y) || bad_opt(router_bias) ||
+      bad_opt(score_bias) ||
       bad_opt(topk_idx) || bad_opt(topk_w) || bad_opt(counts) || bad_opt(drops) ||
       bad_opt(mean_prob))
     return MOE_ERR_INVALID_ARG;
@@ -346,8 +371,8 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
   LogitsView view{};
   MOE_TRY_CUDA(launch_router(c, x, w_router, router_bias, z, &view, status, s, &lc));
   MOE_TRY_CUDA(mark(MOE_STAGE_TOPK));
-  MOE_TRY_CUDA(launch_topk(c, view, nullptr, idx, g, at<float>(ws, L.mp_partial), mean_prob, s,
-                           &lc));
+  MOE_TRY_CUDA(launch_topk(c, view, score_bias, nullptr, idx, g, at<float>(ws, L.mp_partial),
+                           mean_prob, s, &lc));
   MOE_TRY_CUDA(mark(MOE_STAGE_DISPATCH));
   MOE_TRY_CUDA(launch_dispatch(c, idx, at<int32_t>(ws, L.block_hist),
                                at<int32_t>(ws, L.block_base), cnt, drp, offsets, perm, row_of,
@@ -387,19 +412,20 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
 extern "C" {
 
 moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const void* w_router,
-                               const float* router_bias, const void* w_gate, const void* w_up,
+                               const float* router_bias, const float* score_bias,
+                               const void* w_gate, const void* w_up,
                                const void* w_down, const void* ws_gate, const void* ws_up,
                                const void* ws_down, void* y, int32_t* topk_idx, float* topk_w,
                                int32_t* counts, int32_t* drops, float* mean_prob, void* ws,
                                size_t ws_bytes, void* stream) {
-  return layer_forward_impl(cfg, x, w_router, router_bias, w_gate, w_up, w_down, ws_gate,
-                            ws_up, ws_down, y, topk_idx, topk_w, counts, drops, mean_prob, ws,
-                            ws_bytes, stream, nullptr, nullptr);
+  return layer_forward_impl(cfg, x, w_router, router_bias, score_bias, w_gate, w_up, w_down,
+                            ws_gate, ws_up, ws_down, y, topk_idx, topk_w, counts, drops,
+                            mean_prob, ws, ws_bytes, stream, nullptr, nullptr);
 }
 
 moe_status_t moe_layer_forward_profiled(const moe_config_t* cfg, const void* x,
                                         const void* w_router, const float* router_bias,
-                                        const void* w_gate, const void* w_up,
+                                        const float* score_bias, const void* w_gate, const void* w_up,
                                         const void* w_down, const void* ws_gate,
                                         const void* ws_up, const void* ws_down, void* y,
                                         int32_t* topk_idx, float* topk_w, int32_t* counts,
@@ -409,9 +435,10 @@ moe_status_t moe_layer_forward_profiled(const moe_config_t* cfg, const void* x,
   if (!stage_events) return MOE_ERR_INVALID_ARG;
   for (int i = 0; i <= MOE_NUM_STAGES; ++i)
     if (!stage_events[i]) return MOE_ERR_INVALID_ARG;
-  return layer_forward_impl(cfg, x, w_router, router_bias, w_gate, w_up, w_down, ws_gate,
-                            ws_up, ws_down, y, topk_idx, topk_w, counts, drops, mean_prob, ws,
-                            ws_bytes, stream, (cudaEvent_t*)stage_events, n_launches);
+  return layer_forward_impl(cfg, x, w_router, router_bias, score_bias, w_gate, w_up, w_down,
+                            ws_gate, ws_up, ws_down, y, topk_idx, topk_w, counts, drops,
+                            mean_prob, ws, ws_bytes, stream, (cudaEvent_t*)stage_events,
+                            n_launches);
 }
 
 moe_status_t moe_get_error(const void* ws, void* stream) {

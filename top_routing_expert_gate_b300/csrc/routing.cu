@@ -8,6 +8,12 @@
 //   routed_scaling_factor (2.5 for DeepSeek-V3).
 // The selection compares the fp32 logits (softmax and sigmoid are increasing
 // in z) with ties going to the lower expert index.
+//
+// DeepSeek-V3 auxiliary-loss-free routing (same page, "DeepSeek-V3 的无辅助
+// 损失偏置"): with a selection-only score bias b or expert groups, the ranking
+// key is s + b; a group is scored by the sum of its two largest keys, the
+// best topk_group groups are kept, and the experts are chosen among them.
+// The weights always use the raw scores s.
 #include "internal.cuh"
 
 #include <math.h>
@@ -92,13 +98,16 @@ __device__ __forceinline__ bool ranks_before(float za, int ea, float zb, int eb)
 // Block b owns tokens [b*tpb, (b+1)*tpb) so the mean-probability partial of
 // each block is a fixed-order sum, and the final reduction over blocks is too.
 // ---------------------------------------------------------------------------
-template <int EPL>
+// SCORE_KEY: rank by s + score_bias (and expert groups) instead of the logit.
+template <int EPL, bool SCORE_KEY>
 __global__ void __launch_bounds__(256)
 topk_gate_kernel(const float* __restrict__ partials, int splits, size_t split_stride,
-                 const float* __restrict__ bias, float* __restrict__ logits_out, int T, int E,
+                 const float* __restrict__ bias, const float* __restrict__ sbias,
+                 int n_group, int topk_group, float* __restrict__ logits_out, int T, int E,
                  int k, int gate, int renorm, float rsf, int tpb, int32_t* __restrict__ idx_out,
                  float* __restrict__ w_out, float* __restrict__ mp_partial) {
   __shared__ float red[8][kMaxExperts];
+  __shared__ float keys[SCORE_KEY ? 8 : 1][SCORE_KEY ? kMaxExperts : 1];   // per-warp ranking keys
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float acc[EPL];
 #pragma unroll
@@ -144,6 +153,62 @@ topk_gate_kernel(const float* __restrict__ partials, int splits, size_t split_st
 #pragma unroll
     for (int i = 0; i < EPL; ++i) acc[i] += sc[i];
 
+    // ranking value of each of this lane's experts, and the kept groups
+    float rv[EPL];
+    uint32_t gkeep = 0xffffffffu;
+    int gsize = E;
+    if (SCORE_KEY) {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        rv[i] = e < E ? sc[i] + (sbias ? sbias[e] : 0.f) : -INFINITY;
+      }
+      if (n_group > 1) {
+        gsize = E / n_group;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          const int e = lane + 32 * i;
+          if (e < E) keys[warp][e] = rv[i];
+        }
+        __syncwarp();
+        // lane g scores group g: its two largest keys, added
+        float gsc = -INFINITY;
+        if (lane < n_group) {
+          float t1 = -INFINITY, t2 = -INFINITY;
+          for (int e = lane * gsize; e < (lane + 1) * gsize; ++e) {
+            const float v = keys[warp][e];
+            if (v > t1) {
+              t2 = t1;
+              t1 = v;
+            } else if (v > t2) {
+              t2 = v;
+            }
+          }
+          gsc = t1 + t2;
+        }
+        gkeep = 0;
+        for (int r = 0; r < topk_group; ++r) {
+          const bool cand = lane < n_group && !((gkeep >> lane) & 1u);
+          float bz = cand ? gsc : -INFINITY;
+          int be = cand ? lane : 0x7fffffff;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const float oz = __shfl_xor_sync(0xffffffffu, bz, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            if (ranks_before(oz, oe, bz, be)) {
+              bz = oz;
+              be = oe;
+            }
+          }
+          gkeep |= 1u << (be & 31);
+        }
+        __syncwarp();   // keys[warp] is rewritten by the next token
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) rv[i] = zv[i];
+    }
+
     unsigned selmask = 0;
     int my_e = 0;
     float my_s = 0.f;
@@ -153,8 +218,9 @@ topk_gate_kernel(const float* __restrict__ partials, int splits, size_t split_st
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
-        if (e < E && !((selmask >> i) & 1u) && ranks_before(zv[i], e, bz, be)) {
-          bz = zv[i];
+        const bool allowed = !SCORE_KEY || ((gkeep >> (e / gsize)) & 1u);
+        if (e < E && allowed && !((selmask >> i) & 1u) && ranks_before(rv[i], e, bz, be)) {
+          bz = rv[i];
           be = e;
         }
       }
@@ -203,6 +269,28 @@ topk_gate_kernel(const float* __restrict__ partials, int splits, size_t split_st
   }
 }
 
+// One step of the auxiliary-loss-free bias: b_e -= gamma * sign(E * load_e -
+// sum load), load = counts (+ drops), compared in integers.  One block.
+__global__ void __launch_bounds__(kMaxExperts)
+score_bias_update_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ drops,
+                         int E, float gamma, float* __restrict__ bias) {
+  __shared__ long long part[kMaxExperts / 32];
+  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  const long long load = e < E ? (long long)counts[e] + (drops ? (long long)drops[e] : 0) : 0;
+  long long s = load;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) part[warp] = s;
+  __syncthreads();
+  long long total = 0;
+  for (int w = 0; w < kMaxExperts / 32; ++w) total += part[w];
+  if (e < E) {
+    const long long diff = (long long)E * load - total;
+    if (diff > 0) bias[e] -= gamma;
+    else if (diff < 0) bias[e] += gamma;
+  }
+}
+
 __global__ void mean_prob_finalize_kernel(const float* __restrict__ mp_partial, int nblocks,
                                           int E, int T, float* __restrict__ mean_prob) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
@@ -239,9 +327,16 @@ cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_ro
   return cudaGetLastError();
 }
 
-cudaError_t launch_topk(const moe_config_t& c, const LogitsView& z, float* logits_out,
-                        int32_t* idx, float* w, float* mp_partial, float* mean_prob,
-                        cudaStream_t s, LaunchCounter* lc) {
+cudaError_t launch_score_bias_update(const moe_config_t& c, const int32_t* counts,
+                                     const int32_t* drops, float gamma, float* bias,
+                                     cudaStream_t s) {
+  score_bias_update_kernel<<<1, kMaxExperts, 0, s>>>(counts, drops, c.n_experts, gamma, bias);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const moe_config_t& c, const LogitsView& z, const float* score_bias,
+                        float* logits_out, int32_t* idx, float* w, float* mp_partial,
+                        float* mean_prob, cudaStream_t s, LaunchCounter* lc) {
   const int T = c.T, E = c.n_experts;
   if (T == 0) {
     if (mean_prob) return cudaMemsetAsync(mean_prob, 0, sizeof(float) * E, s);
@@ -252,15 +347,24 @@ cudaError_t launch_topk(const moe_config_t& c, const LogitsView& z, float* logit
   const int tpb = (T + nblocks - 1) / nblocks;
   nblocks = (T + tpb - 1) / tpb;
   float* part = mean_prob ? mp_partial : nullptr;
-#define MOE_TOPK_LAUNCH(EPL)                                                              \
-  topk_gate_kernel<EPL><<<nblocks, 256, 0, s>>>(z.partials, z.splits, z.split_stride,   \
-                                                 z.bias, logits_out, T, E, c.top_k,      \
-                                                 c.gate, c.renormalize,                  \
-                                                 c.routed_scaling_factor, tpb, idx, w, part)
-  if (E <= 32) MOE_TOPK_LAUNCH(1);
-  else if (E <= 64) MOE_TOPK_LAUNCH(2);
-  else if (E <= 128) MOE_TOPK_LAUNCH(4);
-  else MOE_TOPK_LAUNCH(8);
+  const bool score_key = score_bias != nullptr || c.n_group > 1;
+  const int ng = c.n_group > 1 ? c.n_group : 1;
+#define MOE_TOPK_LAUNCH(EPL, SK)                                                          \
+  topk_gate_kernel<EPL, SK><<<nblocks, 256, 0, s>>>(                                     \
+      z.partials, z.splits, z.split_stride, z.bias, score_bias, ng, c.topk_group,        \
+      logits_out, T, E, c.top_k, c.gate, c.renormalize, c.routed_scaling_factor, tpb,    \
+      idx, w, part)
+#define MOE_TOPK_EPL(SK)                   \
+  if (E <= 32) MOE_TOPK_LAUNCH(1, SK);     \
+  else if (E <= 64) MOE_TOPK_LAUNCH(2, SK);  \
+  else if (E <= 128) MOE_TOPK_LAUNCH(4, SK); \
+  else MOE_TOPK_LAUNCH(8, SK);
+  if (score_key) {
+    MOE_TOPK_EPL(true)
+  } else {
+    MOE_TOPK_EPL(false)
+  }
+#undef MOE_TOPK_EPL
 #undef MOE_TOPK_LAUNCH
   count_launch(lc);
   cudaError_t err = cudaGetLastError();

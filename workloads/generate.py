@@ -13,6 +13,8 @@ Recipe (one torch.Generator stream per tensor, seeded from the tensor's name):
   unnormalised Zipf(s) mass, so expert 0 is the hottest.  The normaliser of
   the Zipf pmf would cancel under softmax and under the argmax, so it is left
   out.
+* score_bias (shapes with score_bias_std): ~ N(0, std^2) [E] fp32, standing in
+  for a selection-only bias after some training steps of +-gamma.
 
 Values are drawn in float32 and then cast to the shape's dtype (bf16 or fp32).
 This module holds no routing or expert arithmetic.
@@ -64,6 +66,11 @@ def make_inputs(shape: MoEShape, device="cpu", seed: int = 0,
         out["router_bias"] = (-shape.zipf_s * torch.log(e + 1.0)).to(torch.float32).to(device)
     else:
         out["router_bias"] = None
+    if getattr(shape, "score_bias_std", None):
+        out["score_bias"] = _normal((E,), shape.score_bias_std, "score_bias", seed, device,
+                                    torch.float32)
+    else:
+        out["score_bias"] = None
     if with_experts:
         wg = torch.empty((E, F, d), dtype=dt, device=device)
         wu = torch.empty((E, F, d), dtype=dt, device=device)

@@ -11,6 +11,9 @@ Each shape follows a model configuration that the pages describe:
   experts of d_ff 2048, top-8, one always-on shared expert, sigmoid gating,
   renormalisation times routed_scaling_factor 2.5 (same page, sections
   "路由器怎样选专家：top-k 与两种门控" and "细粒度专家与共享专家").
+* ``dsv3_prefill_noaux`` - the same layer routed the way DeepSeek-V3 routes:
+  ranking by sigmoid score plus a selection-only bias, with 8 expert groups of
+  which each token may use 4 (same page, "DeepSeek-V3 的无辅助损失偏置").
 * ``switch`` - a Switch-Transformer-style top-1 layer with an expert capacity
   of ceil(T/E x 1.25) and token dropping (same page, section
   "负载不均：路由坍缩与丢 token"), with a Zipf-skewed router bias so that the
@@ -40,6 +43,9 @@ class MoEShape:
     capacity_factor: Optional[float]   # None = unlimited capacity
     zipf_s: Optional[float]            # router bias skew exponent, None = no bias
     dtype: str        # "fp32" or "bf16" (activations and weights)
+    n_group: int = 0  # expert groups for group-limited selection (0 = none)
+    topk_group: int = 0               # groups kept per token
+    score_bias_std: Optional[float] = None   # selection-only score bias ~ N(0, std^2)
 
     def with_tokens(self, T: int) -> "MoEShape":
         return replace(self, T=T)
@@ -62,6 +68,12 @@ SHAPES = {
     "switch": MoEShape("switch", T=16384, d=2048, E=64, k=1, F=8192, F_s=0,
                        gate="softmax", renormalize=False, rsf=1.0,
                        capacity_factor=1.25, zipf_s=1.2, dtype="bf16"),
+    # DeepSeek-V3's own router ("DeepSeek-V3 的无辅助损失偏置"): rank by
+    # s + b with a selection-only bias, 8 groups of 32 experts, 4 kept
+    "dsv3_prefill_noaux": MoEShape("dsv3_prefill_noaux", T=8192, d=7168, E=256, k=8, F=2048,
+                                   F_s=2048, gate="sigmoid", renormalize=True, rsf=2.5,
+                                   capacity_factor=None, zipf_s=None, dtype="bf16",
+                                   n_group=8, topk_group=4, score_bias_std=0.02),
     "dsv3_decode": MoEShape("dsv3_decode", T=64, d=7168, E=256, k=8, F=2048,
                             F_s=2048, gate="sigmoid", renormalize=True, rsf=2.5,
                             capacity_factor=None, zipf_s=None, dtype="bf16"),
