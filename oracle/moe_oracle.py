@@ -320,7 +320,8 @@ def moe_layer_forward(x: np.ndarray, w_router: np.ndarray, experts,
                       tokens: Optional[Sequence[int]] = None,
                       logits: Optional[np.ndarray] = None,
                       score_bias: Optional[np.ndarray] = None,
-                      n_group: int = 1, topk_group: int = 1) -> Dict[str, np.ndarray]:
+                      n_group: int = 1, topk_group: int = 1,
+                      shared_gate: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
     """Per-expert grouped formulation (the block sketch's loop over experts).
 
     ``experts[e]`` returns (w_gate_e, w_up_e, w_down_e) as float64 arrays and
@@ -328,7 +329,10 @@ def moe_layer_forward(x: np.ndarray, w_router: np.ndarray, experts,
     expert's (w_gate, w_up, w_down).  Routing is always computed for the
     whole batch (capacity depends on earlier tokens); the output y is
     computed for ``tokens`` only (default: all), in that order.  ``logits``,
-    when given, replaces x . W^T (+ bias).
+    when given, replaces x . W^T (+ bias).  ``shared_gate`` (a [d] vector)
+    scales the shared expert's output per token by sigmoid(x_t . w) ([moe10]
+    "细粒度专家与共享专家": a token-dependent sigmoid gate in front of the
+    shared expert); without it the shared output is added with weight 1.
     """
     x = np.asarray(x, dtype=np.float64)
     T = x.shape[0]
@@ -354,10 +358,18 @@ def moe_layer_forward(x: np.ndarray, w_router: np.ndarray, experts,
         for i, (t, j) in enumerate(zip(rows, slots)):
             y[pos[t]] += g[t, j] * out[i]
     if shared is not None:
-        y += swiglu_ffn(x[toks], *shared)
+        sy = swiglu_ffn(x[toks], *shared)
+        if shared_gate is not None:
+            sy = shared_gate_weights(x[toks], shared_gate)[:, None] * sy
+        y += sy
     r["y"] = y
     r["tokens"] = toks
     return r
+
+
+def shared_gate_weights(x_rows: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """Per-token weight of the shared expert: sigmoid(x_t . w)."""
+    return sigmoid(np.asarray(x_rows, np.float64) @ np.asarray(w, np.float64))
 
 
 def moe_layer_forward_token_loop(x: np.ndarray, w_router: np.ndarray, experts,
@@ -365,7 +377,8 @@ def moe_layer_forward_token_loop(x: np.ndarray, w_router: np.ndarray, experts,
                                  routed_scaling_factor: float = 1.0,
                                  capacity: Optional[int] = None,
                                  router_bias: Optional[np.ndarray] = None,
-                                 shared=None) -> np.ndarray:
+                                 shared=None,
+                                 shared_gate: Optional[np.ndarray] = None) -> np.ndarray:
     """Second formulation: per token, per choice, no grouping or permutation.
 
     Used only to cross-check ``moe_layer_forward`` on small inputs; both must
@@ -389,7 +402,10 @@ def moe_layer_forward_token_loop(x: np.ndarray, w_router: np.ndarray, experts,
             wg, wu, wd = experts[e]
             y[t] += g[t, j] * swiglu_ffn(x[t:t + 1], wg, wu, wd)[0]
         if shared is not None:
-            y[t] += swiglu_ffn(x[t:t + 1], *shared)[0]
+            gate = 1.0
+            if shared_gate is not None:
+                gate = 1.0 / (1.0 + math.exp(-float(np.dot(x[t], shared_gate))))
+            y[t] += gate * swiglu_ffn(x[t:t + 1], *shared)[0]
     return y
 
 
@@ -401,6 +417,13 @@ def load_fractions(counts: np.ndarray, drops: np.ndarray) -> np.ndarray:
     """f_e = share of all assignments that chose expert e (kept + dropped)."""
     load = np.asarray(counts, dtype=np.float64) + np.asarray(drops, dtype=np.float64)
     return load / np.sum(load)
+
+
+def balance_loss(counts: np.ndarray, drops: np.ndarray, mean_prob: np.ndarray,
+                 alpha: float) -> float:
+    """L_aux = alpha * N * sum_i f_i * P_i ([moe10] "辅助损失"), from the emitted
+    per-expert counts, drops and mean router probabilities."""
+    return alpha * switch_balance_term(load_fractions(counts, drops), mean_prob)
 
 
 def switch_balance_term(f: np.ndarray, P: np.ndarray) -> float:

@@ -454,3 +454,61 @@ def test_deepseek_v3_groups_limit_each_token_to_four_groups():
     s = O.sigmoid(rng.normal(size=(40, 256)))
     idx = O.topk_experts_biased(s, rng.normal(scale=0.01, size=256), 8, 8, 4)
     assert all(len(set(int(e) // 32 for e in row)) <= 4 for row in idx)
+
+
+# ---------------------------------------------------------------------------
+# Shared-expert gate ([moe10] "细粒度专家与共享专家") and the balance loss scalar
+# ([moe10] "辅助损失")
+# ---------------------------------------------------------------------------
+
+def _tiny_layer(seed, T=24, d=16, E=4, F=8, Fs=8):
+    rng = np.random.default_rng(seed)
+    x = rng.normal(size=(T, d))
+    wr = rng.normal(size=(E, d)) / 4
+    ex = [(rng.normal(size=(F, d)) / 4, rng.normal(size=(F, d)) / 4, rng.normal(size=(d, F)) / 3)
+          for _ in range(E)]
+    sh = (rng.normal(size=(Fs, d)) / 4, rng.normal(size=(Fs, d)) / 4, rng.normal(size=(d, Fs)) / 3)
+    return x, wr, ex, sh
+
+
+def test_shared_gate_zero_weights_halves_shared_expert():
+    # sigmoid(0) = 1/2 exactly: the gated layer equals routed + S(x) / 2
+    x, wr, ex, sh = _tiny_layer(8)
+    full = O.moe_layer_forward(x, wr, ex, k=2, gate="sigmoid", renormalize=True,
+                               routed_scaling_factor=2.5, shared=sh)["y"]
+    gated = O.moe_layer_forward(x, wr, ex, k=2, gate="sigmoid", renormalize=True,
+                                routed_scaling_factor=2.5, shared=sh,
+                                shared_gate=np.zeros(x.shape[1]))["y"]
+    np.testing.assert_allclose(gated, full - 0.5 * O.swiglu_ffn(x, *sh), rtol=1e-12, atol=1e-12)
+
+
+def test_shared_gate_closed_value():
+    # x . w = ln 3 gives the weight 3/4
+    d = 5
+    x = np.zeros((1, d))
+    x[0, 2] = math.log(3.0)
+    w = np.zeros(d)
+    w[2] = 1.0
+    assert O.shared_gate_weights(x, w)[0] == pytest.approx(0.75, abs=1e-15)
+
+
+def test_shared_gate_two_formulations_agree():
+    x, wr, ex, sh = _tiny_layer(9)
+    wsg = np.random.default_rng(10).normal(size=x.shape[1]) / 4
+    a = O.moe_layer_forward(x, wr, ex, k=2, gate="softmax", renormalize=True, shared=sh,
+                            shared_gate=wsg)["y"]
+    b = O.moe_layer_forward_token_loop(x, wr, ex, k=2, gate="softmax", renormalize=True,
+                                       shared=sh, shared_gate=wsg)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+def test_balance_loss_worked_values(golden):
+    # the page's three cases through counts/drops and mean probabilities:
+    # 8 assignments on 4 experts, alpha = 0.01
+    for counts, P, want in [([2, 2, 2, 2], [0.25] * 4, 1.0), ([5, 1, 1, 1], [0.55, 0.15, 0.15, 0.15], 1.6),
+                            ([8, 0, 0, 0], [1, 0, 0, 0], 4.0)]:
+        assert O.balance_loss(np.array(counts), np.zeros(4), np.array(P), 0.01) == \
+            pytest.approx(0.01 * want, rel=1e-12)
+    # dropped assignments still count as assigned
+    assert O.balance_loss(np.array([3, 1, 1, 1]), np.array([2, 0, 0, 0]),
+                          np.array([0.55, 0.15, 0.15, 0.15]), 1.0) == pytest.approx(1.6, rel=1e-12)
