@@ -332,8 +332,8 @@ def main(argv=None):
     def step(evs):
         return moe.moe_layer_forward_profiled(cfg, x, w.w_router, w.router_bias, w.score_bias,
                                               w.w_gate, w.w_up, w.w_down, w.ws_gate, w.ws_up,
-                                              w.ws_down, y, topk_idx, topk_w, counts, drops,
-                                              mean_prob, ws, evs, stream)
+                                              w.ws_down, w.shared_gate, y, topk_idx, topk_w,
+                                              counts, drops, mean_prob, ws, evs, stream)
 
     for _ in range(args.warmup):
         step(warm_events)

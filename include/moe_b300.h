@@ -227,26 +227,53 @@ MOE_API moe_status_t moe_grouped_swiglu(const moe_config_t* cfg, const void* x,
 
 /* Weighted unpermute-combine:
  *   y[t, :] = sum_{j: drop_mask[t*k+j] == 0} topk_w[t, j] * y_perm[row(t*k+j), :]
- *             + y_shared[t, :]   (if y_shared != NULL)
- * where row(a) is the r with perm[r] == a.  Summed in fp32 in ascending j,
+ *             + w_s[t] * y_shared[t, :]   (if y_shared != NULL)
+ * where row(a) is the r with perm[r] == a and w_s[t] = shared_weight[t]
+ * (fp32 [T], e.g. from moe_shared_gate_weights) or 1 when shared_weight is
+ * NULL (shared_weight requires y_shared).  Summed in fp32 in ascending j,
  * then the shared term; written once as out_dtype.  Tokens whose choices were
- * all dropped get y_shared[t] or 0: y excludes the residual. */
+ * all dropped get the shared term or 0: y excludes the residual. */
 MOE_API moe_status_t moe_combine(const moe_config_t* cfg, const float* y_perm, const float* topk_w,
                          const int32_t* offsets, const int32_t* perm,
-                         const uint8_t* drop_mask, const float* y_shared, void* y,
+                         const uint8_t* drop_mask, const float* y_shared,
+                         const float* shared_weight, void* y,
                          void* ws, size_t ws_bytes, void* stream);
+
+/* Per-token weight of the shared expert, weights[t] = sigmoid(x_t . w)
+ * ("10. 混合专家 MoE", section "细粒度专家与共享专家": a sigmoid gate decided
+ * by the current token scales the shared expert's output).
+ *   x [T, d] act_dtype; shared_gate [d] act_dtype (the gate's d -> 1 weight);
+ *   weights [T] fp32 device.  fp32 accumulation in a fixed order. */
+MOE_API moe_status_t moe_shared_gate_weights(const moe_config_t* cfg, const void* x,
+                                             const void* shared_gate, float* weights,
+                                             void* stream);
+
+/* The balance-loss scalar of "10. 混合专家 MoE", section "辅助损失":
+ *   *loss = alpha * E * sum_e f_e * P_e,
+ *   f_e = (counts[e] + drops[e]) / sum_e' (counts[e'] + drops[e'])  (the share
+ *         of assignments that chose e, dropped ones included; drops may be NULL),
+ *   P_e = mean_prob[e]  (as written by moe_router_topk / the layer forward).
+ * counts, drops [E] int32, mean_prob [E] fp32, loss [1] fp32, all device; one
+ * small kernel on `stream`.  0 when there are no assignments. */
+MOE_API moe_status_t moe_balance_loss(const moe_config_t* cfg, const int32_t* counts,
+                                      const int32_t* drops, const float* mean_prob, float alpha,
+                                      float* loss, void* stream);
 
 /* The whole layer forward, stream-ordered, with no host synchronisation:
  * router -> gating/top-k -> capacity/dispatch -> gather -> grouped gate/up +
  * SwiGLU -> grouped down -> combine.
  *   y [T, d] out_dtype (required);
  *   router_bias, score_bias, ws_gate/ws_up/ws_down (all or none) may be NULL;
+ *   shared_gate [d] act_dtype or NULL: when given (requires the shared
+ *     expert), the shared expert's output is scaled per token by
+ *     sigmoid(x_t . shared_gate) (moe_shared_gate_weights);
  *   topk_idx [T, k], topk_w [T, k], counts [E], drops [E], mean_prob [E]
  *     are optional outputs (NULL = not returned). */
 MOE_API moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const void* w_router,
                                const float* router_bias, const float* score_bias,
                                const void* w_gate, const void* w_up, const void* w_down,
                                const void* ws_gate, const void* ws_up, const void* ws_down,
+                               const void* shared_gate,
                                void* y, int32_t* topk_idx, float* topk_w,
                                int32_t* counts, int32_t* drops, float* mean_prob,
                                void* ws, size_t ws_bytes, void* stream);
@@ -271,9 +298,10 @@ typedef enum {
  * moe_layer_forward. */
 MOE_API moe_status_t moe_layer_forward_profiled(
     const moe_config_t* cfg, const void* x, const void* w_router, const float* router_bias,
-    const float* score_bias, const void* w_gate, const void* w_up, const void* w_down, const void* ws_gate,
-    const void* ws_up, const void* ws_down, void* y, int32_t* topk_idx, float* topk_w,
-    int32_t* counts, int32_t* drops, float* mean_prob, void* ws, size_t ws_bytes, void* stream,
+    const float* score_bias, const void* w_gate, const void* w_up, const void* w_down,
+    const void* ws_gate, const void* ws_up, const void* ws_down, const void* shared_gate,
+    void* y, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* drops,
+    float* mean_prob, void* ws, size_t ws_bytes, void* stream,
     void** stage_events, int32_t* n_launches);
 
 /* Self-test of the device-side failure detection.  Every wait inside the

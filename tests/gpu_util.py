@@ -80,7 +80,8 @@ def oracle_layer(shape, inputs, tokens: Optional[Sequence[int]] = None):
         routed_scaling_factor=shape.rsf, capacity=oracle_capacity(shape, T),
         router_bias=to_f64(inputs["router_bias"]), shared=shared_weights(inputs),
         tokens=tokens, score_bias=to_f64(inputs.get("score_bias")),
-        n_group=max(shape.n_group, 1), topk_group=shape.topk_group)
+        n_group=max(shape.n_group, 1), topk_group=shape.topk_group,
+        shared_gate=to_f64(inputs.get("shared_gate")))
 
 
 def biased_margins(scores: np.ndarray, bias: Optional[np.ndarray], idx: np.ndarray,

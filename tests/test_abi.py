@@ -132,18 +132,27 @@ def test_entry_points_reject_missing_workspace_and_pointers():
                             None) == B.MOE_ERR_INVALID_ARG
     # layer: shared weights given although d_ff_shared == 0
     assert lib.moe_layer_forward(ctypes.byref(cfg), fake, fake, None, None, fake, fake, fake, fake,
-                                 fake, fake, fake, None, None, None, None, None, fake, need,
+                                 fake, fake, None, fake, None, None, None, None, None, fake, need,
                                  None) == B.MOE_ERR_INVALID_ARG
     # layer: only some shared weights
     cs = _cfg(F_s=128)
     _, need_s = _ws_size(cs)
     assert lib.moe_layer_forward(ctypes.byref(cs), fake, fake, None, None, fake, fake, fake, fake,
-                                 None, fake, fake, None, None, None, None, None, fake, need_s,
-                                 None) == B.MOE_ERR_INVALID_ARG
+                                 None, fake, None, fake, None, None, None, None, None, fake,
+                                 need_s, None) == B.MOE_ERR_INVALID_ARG
+    # layer: a shared-expert gate without a shared expert
+    assert lib.moe_layer_forward(ctypes.byref(cfg), fake, fake, None, None, fake, fake, fake,
+                                 None, None, None, fake, fake, None, None, None, None, None,
+                                 fake, need, None) == B.MOE_ERR_INVALID_ARG
     # null config
     assert lib.moe_layer_forward(None, fake, fake, None, None, fake, fake, fake, None, None, None,
-                                 fake, None, None, None, None, None, fake, need,
+                                 None, fake, None, None, None, None, None, fake, need,
                                  None) == B.MOE_ERR_INVALID_ARG
+    # balance loss / shared gate: null outputs
+    assert lib.moe_balance_loss(ctypes.byref(cfg), fake, None, fake, 0.01, None,
+                                None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_shared_gate_weights(ctypes.byref(cfg), fake, None, fake,
+                                       None) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_get_error(None, None) == B.MOE_ERR_WORKSPACE
     # misaligned selection bias
     assert lib.moe_topk_from_logits(ctypes.byref(cfg), fake, fake + 4, fake, fake, None, fake,

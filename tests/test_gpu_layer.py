@@ -55,6 +55,9 @@ MID_SHAPES = {
     # N tail (d = 320 is one full 256-column tile plus 64 columns)
     "mid_multi_mtile": _shape(T=1000, d=320, E=4, k=2, F=256, F_s=128),
     "mid_wide_ff": _shape(T=520, d=128, E=3, k=1, F=1024, gate="sigmoid", rsf=2.5),
+    # the shared expert behind a per-token sigmoid gate
+    "mid_gated_shared": _shape(T=333, d=256, E=16, k=4, F=256, F_s=256, gate="sigmoid",
+                               rsf=2.5, shared_gate=True),
 }
 
 
@@ -161,11 +164,68 @@ def test_deterministic_and_split_calls_match_fused():
                            w.w_down, w.ws_gate, w.ws_up, w.ws_down, y_perm, y_sh, ws)
     y = torch.empty((s.T, s.d), dtype=torch.float32, device=DEV)
     moe.moe_combine(cfg, y_perm, r["topk_w"], dsp["offsets"], dsp["perm"], dsp["drop_mask"],
-                    y_sh, y, ws)
+                    y_sh, None, y, ws)
     torch.cuda.synchronize()
     assert torch.equal(r["topk_idx"], a["topk_idx"])
     assert torch.equal(y, a["y"])
     assert moe.moe_get_error(ws) == 0
+
+
+def test_gated_shared_expert_split_calls_match_fused():
+    s = MID_SHAPES["mid_gated_shared"]
+    inp = make_inputs(s, device=DEV, seed=7)
+    cfg = moe.config_from_shape(s)
+    ws = moe.Workspace(cfg)
+    w = moe.LayerWeights.from_inputs(inp)
+    a = moe.layer_forward(cfg, inp["x"], w, ws=ws)
+    r = moe.route(cfg, inp["x"], w.w_router, w.router_bias, ws=ws)
+    dsp = moe.dispatch(cfg, r["topk_idx"], ws=ws)
+    A = s.T * s.k
+    y_perm = torch.empty((A, s.d), dtype=torch.float32, device=DEV)
+    y_sh = torch.empty((s.T, s.d), dtype=torch.float32, device=DEV)
+    moe.moe_grouped_swiglu(cfg, inp["x"], dsp["perm"], dsp["offsets"], w.w_gate, w.w_up,
+                           w.w_down, w.ws_gate, w.ws_up, w.ws_down, y_perm, y_sh, ws)
+    gate_w = torch.empty(s.T, dtype=torch.float32, device=DEV)
+    moe.moe_shared_gate_weights(cfg, inp["x"], w.shared_gate, gate_w)
+    y = torch.empty((s.T, s.d), dtype=torch.float32, device=DEV)
+    moe.moe_combine(cfg, y_perm, r["topk_w"], dsp["offsets"], dsp["perm"], dsp["drop_mask"],
+                    y_sh, gate_w, y, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y, a["y"])
+    # the gate weights themselves: sigmoid(x . w), fp32 accumulation of d bf16 products
+    want = O.shared_gate_weights(to_f64(inp["x"]), to_f64(w.shared_gate))
+    np.testing.assert_allclose(np_f(gate_w), want, rtol=0, atol=2e-6)
+    assert moe.moe_get_error(ws) == 0
+
+
+@pytest.mark.parametrize("counts,drops,P,want", [
+    ([2, 2, 2, 2], [0, 0, 0, 0], [0.25, 0.25, 0.25, 0.25], 1.0),
+    ([5, 1, 1, 1], [0, 0, 0, 0], [0.55, 0.15, 0.15, 0.15], 1.6),
+    ([3, 1, 1, 1], [2, 0, 0, 0], [0.55, 0.15, 0.15, 0.15], 1.6),
+    ([8, 0, 0, 0], [0, 0, 0, 0], [1.0, 0.0, 0.0, 0.0], 4.0),
+])
+def test_balance_loss_worked_values_on_gpu(counts, drops, P, want):
+    # "辅助损失": N * sum f P = 1.0 uniform, 1.6 skewed, 4.0 collapsed (alpha = 0.01)
+    cfg = moe.make_config(8, 64, 4, 1, 128, act_dtype="fp32")
+    loss = torch.zeros(1, dtype=torch.float32, device=DEV)
+    moe.moe_balance_loss(cfg, torch.tensor(counts, dtype=torch.int32, device=DEV),
+                         torch.tensor(drops, dtype=torch.int32, device=DEV),
+                         torch.tensor(P, dtype=torch.float32, device=DEV), 0.01, loss)
+    torch.cuda.synchronize()
+    assert loss.item() == pytest.approx(0.01 * want, rel=1e-6)
+
+
+def test_balance_loss_from_layer_statistics():
+    s = MID_SHAPES["mid_capacity_zipf"]
+    inp = make_inputs(s, device=DEV, seed=8)
+    cfg = moe.config_from_shape(s)
+    out = moe.layer_forward(cfg, inp["x"], moe.LayerWeights.from_inputs(inp))
+    loss = torch.zeros(1, dtype=torch.float32, device=DEV)
+    moe.moe_balance_loss(cfg, out["counts"], out["drops"], out["mean_prob"], 0.02, loss)
+    torch.cuda.synchronize()
+    want = O.balance_loss(np_i(out["counts"]), np_i(out["drops"]), np_f(out["mean_prob"]), 0.02)
+    assert loss.item() == pytest.approx(want, rel=1e-6)
+    assert loss.item() > 0.02   # the Zipf skew makes it exceed the balanced minimum alpha
 
 
 # ---------------------------------------------------------------------------

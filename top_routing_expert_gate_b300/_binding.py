@@ -76,16 +76,19 @@ SIGNATURES = {
                                      c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_combine": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                              c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+                              c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "moe_shared_gate_weights": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "moe_balance_loss": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_float, c_void_p,
+                                   c_void_p]),
     "moe_layer_forward": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                    c_void_p, c_void_p, c_size_t, c_void_p]),
+                                    c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_layer_forward_profiled": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p,
                                              c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                              c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                             c_void_p, c_void_p, c_void_p, c_size_t, c_void_p,
-                                             c_void_p, c_void_p]),
+                                             c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                             c_void_p, c_void_p, c_void_p]),
     "moe_get_error": (c_int32, [c_void_p, c_void_p]),
     "moe_selftest_bounded_wait": (c_int32, [c_void_p, c_size_t, ctypes.c_uint64, c_void_p]),
 }

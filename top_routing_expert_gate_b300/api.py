@@ -138,28 +138,41 @@ def moe_grouped_swiglu(cfg, x, perm, offsets, w_gate, w_up, w_down, ws_gate, ws_
         ws.ptr, ws.nbytes, _stream(stream)), "moe_grouped_swiglu")
 
 
-def moe_combine(cfg, y_perm, topk_w, offsets, perm, drop_mask, y_shared, y, ws: Workspace,
-                stream=None) -> None:
+def moe_combine(cfg, y_perm, topk_w, offsets, perm, drop_mask, y_shared, shared_weight, y,
+                ws: Workspace, stream=None) -> None:
     check(load_library().moe_combine(
         ctypes.byref(cfg), _ptr(y_perm), _ptr(topk_w), _ptr(offsets), _ptr(perm),
-        _ptr(drop_mask), _ptr(y_shared), _ptr(y), ws.ptr, ws.nbytes, _stream(stream)),
-        "moe_combine")
+        _ptr(drop_mask), _ptr(y_shared), _ptr(shared_weight), _ptr(y), ws.ptr, ws.nbytes,
+        _stream(stream)), "moe_combine")
+
+
+def moe_shared_gate_weights(cfg, x, shared_gate, weights, stream=None) -> None:
+    check(load_library().moe_shared_gate_weights(
+        ctypes.byref(cfg), _ptr(x, "x"), _ptr(shared_gate, "shared_gate"),
+        _ptr(weights, "weights"), _stream(stream)), "moe_shared_gate_weights")
+
+
+def moe_balance_loss(cfg, counts, drops, mean_prob, alpha: float, loss, stream=None) -> None:
+    check(load_library().moe_balance_loss(
+        ctypes.byref(cfg), _ptr(counts, "counts"), _ptr(drops), _ptr(mean_prob, "mean_prob"),
+        float(alpha), _ptr(loss, "loss"), _stream(stream)), "moe_balance_loss")
 
 
 def moe_layer_forward(cfg, x, w_router, router_bias, score_bias, w_gate, w_up, w_down, ws_gate,
-                      ws_up, ws_down, y, topk_idx, topk_w, counts, drops, mean_prob,
+                      ws_up, ws_down, shared_gate, y, topk_idx, topk_w, counts, drops, mean_prob,
                       ws: Workspace, stream=None) -> None:
     check(load_library().moe_layer_forward(
         ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(score_bias),
-        _ptr(w_gate),
-        _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), _ptr(y),
+        _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down),
+        _ptr(shared_gate), _ptr(y),
         _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(drops), _ptr(mean_prob), ws.ptr,
         ws.nbytes, _stream(stream)), "moe_layer_forward")
 
 
 def moe_layer_forward_profiled(cfg, x, w_router, router_bias, score_bias, w_gate, w_up, w_down,
-                               ws_gate, ws_up, ws_down, y, topk_idx, topk_w, counts, drops,
-                               mean_prob, ws: Workspace, stage_events, stream=None) -> int:
+                               ws_gate, ws_up, ws_down, shared_gate, y, topk_idx, topk_w, counts,
+                               drops, mean_prob, ws: Workspace, stage_events,
+                               stream=None) -> int:
     """moe_layer_forward recording ``stage_events`` (MOE_NUM_STAGES + 1
     torch.cuda.Event with timing, already recorded once so that they exist)
     before each stage; returns the number of kernels the call launched."""
@@ -170,7 +183,7 @@ def moe_layer_forward_profiled(cfg, x, w_router, router_bias, score_bias, w_gate
     check(load_library().moe_layer_forward_profiled(
         ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(score_bias),
         _ptr(w_gate),
-        _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), _ptr(y),
+        _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), _ptr(shared_gate), _ptr(y),
         _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(drops), _ptr(mean_prob), ws.ptr,
         ws.nbytes, _stream(stream), arr, ctypes.byref(n)), "moe_layer_forward_profiled")
     return n.value
@@ -241,12 +254,13 @@ class LayerWeights:
     ws_up: Optional[torch.Tensor] = None
     ws_down: Optional[torch.Tensor] = None
     score_bias: Optional[torch.Tensor] = None
+    shared_gate: Optional[torch.Tensor] = None
 
     @classmethod
     def from_inputs(cls, inputs) -> "LayerWeights":
         return cls(inputs["w_router"], inputs["w_gate"], inputs["w_up"], inputs["w_down"],
                    inputs.get("router_bias"), inputs.get("ws_gate"), inputs.get("ws_up"),
-                   inputs.get("ws_down"), inputs.get("score_bias"))
+                   inputs.get("ws_down"), inputs.get("score_bias"), inputs.get("shared_gate"))
 
 
 def layer_forward(cfg, x, w: LayerWeights, ws: Optional[Workspace] = None,
@@ -261,6 +275,7 @@ def layer_forward(cfg, x, w: LayerWeights, ws: Optional[Workspace] = None,
                    drops=_i32(E, dev), mean_prob=_f32(E, dev))
     g = out.get
     moe_layer_forward(cfg, x, w.w_router, w.router_bias, w.score_bias, w.w_gate, w.w_up,
-                      w.w_down, w.ws_gate, w.ws_up, w.ws_down, out["y"], g("topk_idx"),
+                      w.w_down, w.ws_gate, w.ws_up, w.ws_down, w.shared_gate, out["y"],
+                      g("topk_idx"),
                       g("topk_w"), g("counts"), g("drops"), g("mean_prob"), ws, stream)
     return out

@@ -197,13 +197,13 @@ __device__ __forceinline__ void store4(__nv_bfloat16* y, float4 v) {
 }
 
 // One block per token (grid-stride); fp32 accumulation in ascending j, then
-// the shared expert; one write of y.
+// the shared expert (times its per-token gate when given); one write of y.
 template <typename TOut>
 __global__ void __launch_bounds__(256)
 combine_kernel(const float4* __restrict__ y_perm, const float* __restrict__ topk_w,
                const int32_t* __restrict__ row_of, const uint8_t* __restrict__ drop_mask,
-               const float4* __restrict__ y_shared, TOut* __restrict__ y, int T, int k, int d,
-               int A, int32_t* status) {
+               const float4* __restrict__ y_shared, const float* __restrict__ shared_w,
+               TOut* __restrict__ y, int T, int k, int d, int A, int32_t* status) {
   __shared__ int s_row[kMaxTopK];
   __shared__ float s_g[kMaxTopK];
   const int d4 = d >> 2;
@@ -236,10 +236,18 @@ combine_kernel(const float4* __restrict__ y_perm, const float* __restrict__ topk
       }
       if (y_shared) {
         const float4 sv = __ldg(y_shared + (size_t)t * d4 + v);
-        acc.x += sv.x;
-        acc.y += sv.y;
-        acc.z += sv.z;
-        acc.w += sv.w;
+        if (shared_w) {
+          const float ws = __ldg(shared_w + t);
+          acc.x = fmaf(ws, sv.x, acc.x);
+          acc.y = fmaf(ws, sv.y, acc.y);
+          acc.z = fmaf(ws, sv.z, acc.z);
+          acc.w = fmaf(ws, sv.w, acc.w);
+        } else {
+          acc.x += sv.x;
+          acc.y += sv.y;
+          acc.z += sv.z;
+          acc.w += sv.w;
+        }
       }
       store4(y + (size_t)t * d + 4 * v, acc);
     }
@@ -316,8 +324,8 @@ cudaError_t launch_invert_perm(const moe_config_t& c, const int32_t* perm,
 
 cudaError_t launch_combine(const moe_config_t& c, const float* y_perm, const float* topk_w,
                            const int32_t* row_of, const uint8_t* drop_mask,
-                           const float* y_shared, void* y, int32_t* status, cudaStream_t s,
-                           LaunchCounter* lc) {
+                           const float* y_shared, const float* shared_w, void* y,
+                           int32_t* status, cudaStream_t s, LaunchCounter* lc) {
   const int T = c.T;
   if (T == 0) return cudaSuccess;
   int blocks = T;
@@ -325,11 +333,11 @@ cudaError_t launch_combine(const moe_config_t& c, const float* y_perm, const flo
   const int A = T * c.top_k;
   if (c.out_dtype == MOE_BF16)
     combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
-        (const float4*)y_perm, topk_w, row_of, drop_mask, (const float4*)y_shared,
+        (const float4*)y_perm, topk_w, row_of, drop_mask, (const float4*)y_shared, shared_w,
         (__nv_bfloat16*)y, T, c.top_k, c.d_model, A, status);
   else
     combine_kernel<float><<<blocks, 256, 0, s>>>((const float4*)y_perm, topk_w, row_of,
-                                                 drop_mask, (const float4*)y_shared, (float*)y,
+                                                 drop_mask, (const float4*)y_shared, shared_w, (float*)y,
                                                  T, c.top_k, c.d_model, A, status);
   count_launch(lc);
   return cudaGetLastError();

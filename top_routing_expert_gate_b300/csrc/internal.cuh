@@ -50,6 +50,7 @@ struct WsLayout {
   size_t h_shared;    // [T, F_s] act
   size_t y_perm;      // [A, d] fp32
   size_t y_shared;    // [T, d] fp32
+  size_t shared_w;    // [T] fp32, per-token shared-expert gate
   size_t total;
   int nb;             // dispatch blocks
 };
@@ -111,6 +112,15 @@ cudaError_t launch_topk(const moe_config_t& c, const LogitsView& z, const float*
                         float* logits_out, int32_t* idx, float* w, float* mp_partial,
                         float* mean_prob, cudaStream_t s, LaunchCounter* lc = nullptr);
 
+// out[t] = sigmoid(x_t . w), the per-token weight of the shared expert.
+cudaError_t launch_shared_gate(const moe_config_t& c, const void* x, const void* w, float* out,
+                               cudaStream_t s, LaunchCounter* lc = nullptr);
+
+// *loss = alpha * E * sum_e f_e P_e, f_e = load_e / sum load (load = counts + drops).
+cudaError_t launch_balance_loss(const moe_config_t& c, const int32_t* counts,
+                                const int32_t* drops, const float* mean_prob, float alpha,
+                                float* loss, cudaStream_t s);
+
 // b_e -= gamma * sign(E * load_e - sum load), load = counts (+ drops).
 cudaError_t launch_score_bias_update(const moe_config_t& c, const int32_t* counts,
                                      const int32_t* drops, float gamma, float* bias,
@@ -133,11 +143,12 @@ cudaError_t launch_invert_perm(const moe_config_t& c, const int32_t* perm,
                                const int32_t* offsets, int32_t* row_of, int32_t* status,
                                cudaStream_t s, LaunchCounter* lc = nullptr);
 
-// y[t] = sum_j kept g[t,j] y_perm[row_of[t*k+j]] (+ y_shared[t]).
+// y[t] = sum_j kept g[t,j] y_perm[row_of[t*k+j]] (+ w_s[t] * y_shared[t], w_s = 1 when
+// shared_w is null).
 cudaError_t launch_combine(const moe_config_t& c, const float* y_perm, const float* topk_w,
                            const int32_t* row_of, const uint8_t* drop_mask,
-                           const float* y_shared, void* y, int32_t* status, cudaStream_t s,
-                           LaunchCounter* lc = nullptr);
+                           const float* y_shared, const float* shared_w, void* y,
+                           int32_t* status, cudaStream_t s, LaunchCounter* lc = nullptr);
 
 // Grouped expert GEMMs.  Routed groups take rows offsets[e]..offsets[e+1] of
 // x_perm / h; the shared group (when ws_* given) takes all T rows of x / h_shared.

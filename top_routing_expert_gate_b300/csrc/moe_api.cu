@@ -42,6 +42,7 @@ WsLayout ws_layout(const moe_config_t& c) {
   L.h_shared = take(T * Fs * ab);
   L.y_perm = take(A * d * 4);
   L.y_shared = take(T * d * 4);
+  L.shared_w = take(T * 4);
   L.total = o;
   return L;
 }
@@ -300,13 +301,14 @@ moe_status_t moe_grouped_swiglu(const moe_config_t* cfg, const void* x, const in
 
 moe_status_t moe_combine(const moe_config_t* cfg, const float* y_perm, const float* topk_w,
                          const int32_t* offsets, const int32_t* perm,
-                         const uint8_t* drop_mask, const float* y_shared, void* y, void* ws,
-                         size_t ws_bytes, void* stream) {
+                         const uint8_t* drop_mask, const float* y_shared,
+                         const float* shared_weight, void* y, void* ws, size_t ws_bytes,
+                         void* stream) {
   MOE_TRY(check_config(cfg));
   MOE_TRY(check_ws(cfg, ws, ws_bytes));
   if (bad_ptr(cfg, y_perm) || bad_ptr(cfg, topk_w) || bad_ptr(cfg, perm) ||
       bad_ptr(cfg, drop_mask) || bad_ptr(cfg, y) || !offsets || !aligned16(offsets) ||
-      bad_opt(y_shared))
+      bad_opt(y_shared) || bad_opt(shared_weight) || (shared_weight && !y_shared))
     return MOE_ERR_INVALID_ARG;
   if (cfg->T == 0) return MOE_OK;
   const WsLayout L = ws_layout(*cfg);
@@ -314,8 +316,27 @@ moe_status_t moe_combine(const moe_config_t* cfg, const float* y_perm, const flo
   int32_t* status = at<int32_t>(ws, L.status);
   int32_t* row_of = at<int32_t>(ws, L.row_of);
   MOE_TRY_CUDA(launch_invert_perm(*cfg, perm, offsets, row_of, status, s));
+  return cuda_status(launch_combine(*cfg, y_perm, topk_w, row_of, drop_mask, y_shared,
+                                    shared_weight, y, status, s));
+}
+
+moe_status_t moe_shared_gate_weights(const moe_config_t* cfg, const void* x,
+                                     const void* shared_gate, float* weights, void* stream) {
+  MOE_TRY(check_config(cfg));
+  if (bad_ptr(cfg, x) || bad_ptr(cfg, weights) || !shared_gate || !aligned16(shared_gate))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_shared_gate(*cfg, x, shared_gate, weights, (cudaStream_t)stream));
+}
+
+moe_status_t moe_balance_loss(const moe_config_t* cfg, const int32_t* counts,
+                              const int32_t* drops, const float* mean_prob, float alpha,
+                              float* loss, void* stream) {
+  MOE_TRY(check_config(cfg));
+  if (!counts || !mean_prob || !loss || !aligned16(counts) || !aligned16(mean_prob) ||
+      bad_opt(drops) || ((uintptr_t)loss & 3u) != 0 || !isfinite(alpha))
+    return MOE_ERR_INVALID_ARG;
   return cuda_status(
-      launch_combine(*cfg, y_perm, topk_w, row_of, drop_mask, y_shared, y, status, s));
+      launch_balance_loss(*cfg, counts, drops, mean_prob, alpha, loss, (cudaStream_t)stream));
 }
 
 }  // extern "C"
@@ -328,10 +349,10 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
                                 const float* router_bias, const float* score_bias,
                                 const void* w_gate, const void* w_up,
                                 const void* w_down, const void* ws_gate, const void* ws_up,
-                                const void* ws_down, void* y, int32_t* topk_idx, float* topk_w,
-                                int32_t* counts, int32_t* drops, float* mean_prob, void* ws,
-                                size_t ws_bytes, void* stream, cudaEvent_t* ev,
-                                int32_t* n_launches) {
+                                const void* ws_down, const void* shared_gate, void* y,
+                                int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                int32_t* drops, float* mean_prob, void* ws, size_t ws_bytes,
+                                void* stream, cudaEvent_t* ev, int32_t* n_launches) {
   MOE_TRY(check_config(cfg));
   MOE_TRY(check_ws(cfg, ws, ws_bytes));
   if (bad_ptr(cfg, x) || bad_ptr(cfg, w_router) || bad_ptr(cfg, w_gate) ||
@@ -341,6 +362,7 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
       bad_opt(mean_prob))
     return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_shared_args(cfg, ws_gate, ws_up, ws_down));
+  if (bad_opt(shared_gate) || (shared_gate && !ws_gate)) return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(*cfg);
   cudaStream_t s = (cudaStream_t)stream;
   const moe_config_t& c = *cfg;
@@ -370,6 +392,8 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
   MOE_TRY_CUDA(mark(MOE_STAGE_ROUTER));
   LogitsView view{};
   MOE_TRY_CUDA(launch_router(c, x, w_router, router_bias, z, &view, status, s, &lc));
+  float* shared_w = shared_gate ? at<float>(ws, L.shared_w) : nullptr;
+  if (shared_gate) MOE_TRY_CUDA(launch_shared_gate(c, x, shared_gate, shared_w, s, &lc));
   MOE_TRY_CUDA(mark(MOE_STAGE_TOPK));
   MOE_TRY_CUDA(launch_topk(c, view, score_bias, nullptr, idx, g, at<float>(ws, L.mp_partial),
                            mean_prob, s, &lc));
@@ -401,7 +425,8 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
   a.launches = &lc;
   MOE_TRY_CUDA(run_experts(c, a, s));
   MOE_TRY_CUDA(mark(MOE_STAGE_COMBINE));
-  MOE_TRY_CUDA(launch_combine(c, a.y_perm, g, row_of, dmask, a.y_shared, y, status, s, &lc));
+  MOE_TRY_CUDA(
+      launch_combine(c, a.y_perm, g, row_of, dmask, a.y_shared, shared_w, y, status, s, &lc));
   MOE_TRY_CUDA(mark(MOE_NUM_STAGES));
   if (n_launches) *n_launches = lc.n;
   return MOE_OK;
@@ -415,19 +440,21 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
                                const float* router_bias, const float* score_bias,
                                const void* w_gate, const void* w_up,
                                const void* w_down, const void* ws_gate, const void* ws_up,
-                               const void* ws_down, void* y, int32_t* topk_idx, float* topk_w,
-                               int32_t* counts, int32_t* drops, float* mean_prob, void* ws,
-                               size_t ws_bytes, void* stream) {
+                               const void* ws_down, const void* shared_gate, void* y,
+                               int32_t* topk_idx, float* topk_w, int32_t* counts,
+                               int32_t* drops, float* mean_prob, void* ws, size_t ws_bytes,
+                               void* stream) {
   return layer_forward_impl(cfg, x, w_router, router_bias, score_bias, w_gate, w_up, w_down,
-                            ws_gate, ws_up, ws_down, y, topk_idx, topk_w, counts, drops,
-                            mean_prob, ws, ws_bytes, stream, nullptr, nullptr);
+                            ws_gate, ws_up, ws_down, shared_gate, y, topk_idx, topk_w, counts,
+                            drops, mean_prob, ws, ws_bytes, stream, nullptr, nullptr);
 }
 
 moe_status_t moe_layer_forward_profiled(const moe_config_t* cfg, const void* x,
                                         const void* w_router, const float* router_bias,
-                                        const float* score_bias, const void* w_gate, const void* w_up,
-                                        const void* w_down, const void* ws_gate,
-                                        const void* ws_up, const void* ws_down, void* y,
+                                        const float* score_bias, const void* w_gate,
+                                        const void* w_up, const void* w_down,
+                                        const void* ws_gate, const void* ws_up,
+                                        const void* ws_down, const void* shared_gate, void* y,
                                         int32_t* topk_idx, float* topk_w, int32_t* counts,
                                         int32_t* drops, float* mean_prob, void* ws,
                                         size_t ws_bytes, void* stream, void** stage_events,
@@ -436,8 +463,8 @@ moe_status_t moe_layer_forward_profiled(const moe_config_t* cfg, const void* x,
   for (int i = 0; i <= MOE_NUM_STAGES; ++i)
     if (!stage_events[i]) return MOE_ERR_INVALID_ARG;
   return layer_forward_impl(cfg, x, w_router, router_bias, score_bias, w_gate, w_up, w_down,
-                            ws_gate, ws_up, ws_down, y, topk_idx, topk_w, counts, drops,
-                            mean_prob, ws, ws_bytes, stream, (cudaEvent_t*)stage_events,
+                            ws_gate, ws_up, ws_down, shared_gate, y, topk_idx, topk_w, counts,
+                            drops, mean_prob, ws, ws_bytes, stream, (cudaEvent_t*)stage_events,
                             n_launches);
 }
 

@@ -291,6 +291,48 @@ score_bias_update_kernel(const int32_t* __restrict__ counts, const int32_t* __re
   }
 }
 
+// Per-token weight of the shared expert, sigmoid(x_t . w) ("细粒度专家与共享
+// 专家": a token-dependent sigmoid gate in front of the shared expert).  One
+// warp per token, fp32 accumulation in a fixed order.
+template <typename TIn>
+__global__ void __launch_bounds__(256)
+shared_gate_kernel(const TIn* __restrict__ x, const TIn* __restrict__ w, int T, int d,
+                   float* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const TIn* row = x + (size_t)t * d;
+  float acc = 0.f;
+  for (int c = lane; c < d; c += 32) acc = fmaf(to_f(row[c]), to_f(w[c]), acc);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) out[t] = 1.f / (1.f + expf(-acc));
+}
+
+// alpha * N * sum_e f_e * P_e with f_e = (counts_e + drops_e) / sum of loads
+// ("辅助损失").  One block, fixed-order sums.
+__global__ void __launch_bounds__(kMaxExperts)
+balance_loss_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ drops,
+                    const float* __restrict__ mean_prob, int E, float alpha,
+                    float* __restrict__ loss) {
+  __shared__ double fp[kMaxExperts];
+  __shared__ long long ld[kMaxExperts];
+  const int e = threadIdx.x;
+  const long long load = e < E ? (long long)counts[e] + (drops ? (long long)drops[e] : 0) : 0;
+  ld[e] = load;
+  fp[e] = e < E ? (double)load * (double)mean_prob[e] : 0.0;
+  __syncthreads();
+  if (e == 0) {
+    long long total = 0;
+    double s = 0.0;
+    for (int i = 0; i < E; ++i) {
+      total += ld[i];
+      s += fp[i];
+    }
+    *loss = total > 0 ? (float)((double)alpha * (double)E * s / (double)total) : 0.f;
+  }
+}
+
 __global__ void mean_prob_finalize_kernel(const float* __restrict__ mp_partial, int nblocks,
                                           int E, int T, float* __restrict__ mean_prob) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
@@ -331,6 +373,28 @@ cudaError_t launch_score_bias_update(const moe_config_t& c, const int32_t* count
                                      const int32_t* drops, float gamma, float* bias,
                                      cudaStream_t s) {
   score_bias_update_kernel<<<1, kMaxExperts, 0, s>>>(counts, drops, c.n_experts, gamma, bias);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shared_gate(const moe_config_t& c, const void* x, const void* w, float* out,
+                               cudaStream_t s, LaunchCounter* lc) {
+  if (c.T == 0) return cudaSuccess;
+  const int blocks = (c.T + 7) / 8;
+  if (c.act_dtype == MOE_BF16)
+    shared_gate_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+        (const __nv_bfloat16*)x, (const __nv_bfloat16*)w, c.T, c.d_model, out);
+  else
+    shared_gate_kernel<float><<<blocks, 256, 0, s>>>((const float*)x, (const float*)w, c.T,
+                                                     c.d_model, out);
+  count_launch(lc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_balance_loss(const moe_config_t& c, const int32_t* counts,
+                                const int32_t* drops, const float* mean_prob, float alpha,
+                                float* loss, cudaStream_t s) {
+  balance_loss_kernel<<<1, kMaxExperts, 0, s>>>(counts, drops, mean_prob, c.n_experts, alpha,
+                                                loss);
   return cudaGetLastError();
 }
 

@@ -15,6 +15,7 @@ Recipe (one torch.Generator stream per tensor, seeded from the tensor's name):
   out.
 * score_bias (shapes with score_bias_std): ~ N(0, std^2) [E] fp32, standing in
   for a selection-only bias after some training steps of +-gamma.
+* shared_gate (shapes with a gated shared expert) ~ N(0, 1/d) [d].
 
 Values are drawn in float32 and then cast to the shape's dtype (bf16 or fp32).
 This module holds no routing or expert arithmetic.
@@ -86,6 +87,9 @@ def make_inputs(shape: MoEShape, device="cpu", seed: int = 0,
             out["ws_down"] = _normal((d, Fs), 1.0 / math.sqrt(Fs), "ws_down", seed, device, dt)
         else:
             out["ws_gate"] = out["ws_up"] = out["ws_down"] = None
+        out["shared_gate"] = None
+        if Fs > 0 and getattr(shape, "shared_gate", False):
+            out["shared_gate"] = _normal((d,), 1.0 / math.sqrt(d), "shared_gate", seed, device, dt)
     return out
 
 

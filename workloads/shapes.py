@@ -46,6 +46,7 @@ class MoEShape:
     n_group: int = 0  # expert groups for group-limited selection (0 = none)
     topk_group: int = 0               # groups kept per token
     score_bias_std: Optional[float] = None   # selection-only score bias ~ N(0, std^2)
+    shared_gate: bool = False         # per-token sigmoid gate on the shared expert
 
     def with_tokens(self, T: int) -> "MoEShape":
         return replace(self, T=T)
