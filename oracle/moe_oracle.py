@@ -435,6 +435,32 @@ def switch_balance_term(f: np.ndarray, P: np.ndarray) -> float:
 
 
 # ---------------------------------------------------------------------------
+# FP8 (E4M3) expert weights ([moe10] "推理时：显存按总参数，计算按激活参数":
+# DeepSeek-V3 ships its weights in FP8, about one byte per parameter).  A
+# stored weight is an 8-bit E4M3 code times a per-output-channel scale.
+# E4M3: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0
+# holds the subnormals m * 2^-9; S.1111.111 is NaN (no infinities); the
+# largest finite value is 448.
+# ---------------------------------------------------------------------------
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Value of each E4M3 code (uint8 array), straight from the format."""
+    c = np.asarray(codes, dtype=np.int64)
+    sign = np.where((c >> 7) & 1, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    normal = (1.0 + m / 8.0) * np.power(2.0, e.astype(np.float64) - 7.0)
+    sub = m * 2.0 ** -9
+    v = sign * np.where(e == 0, sub, normal)
+    return np.where((e == 15) & ((c & 7) == 7), np.nan, v)
+
+
+def dequantize_rows(codes, scale) -> np.ndarray:
+    """w[r, c] = e4m3(codes[r, c]) * scale[r] (one scale per output channel)."""
+    return e4m3_to_f64(codes) * np.asarray(scale, dtype=np.float64)[:, None]
+
+
+# ---------------------------------------------------------------------------
 # Parameter accounting ([moe10] "总参数和激活参数怎样算").
 # ---------------------------------------------------------------------------
 

@@ -512,3 +512,36 @@ def test_balance_loss_worked_values(golden):
     # dropped assignments still count as assigned
     assert O.balance_loss(np.array([3, 1, 1, 1]), np.array([2, 0, 0, 0]),
                           np.array([0.55, 0.15, 0.15, 0.15]), 1.0) == pytest.approx(1.6, rel=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 expert weights ([moe10] "推理时": DeepSeek-V3 ships FP8 weights)
+# ---------------------------------------------------------------------------
+
+def test_e4m3_landmark_values():
+    v = O.e4m3_to_f64(np.array([0x38, 0x7E, 0x01, 0x08, 0x07, 0x00, 0x80, 0xB8, 0x40, 0x30]))
+    np.testing.assert_array_equal(v, [1.0, 448.0, 2.0 ** -9, 2.0 ** -6, 7 * 2.0 ** -9, 0.0, -0.0,
+                                      -1.0, 2.0, 0.5])
+    assert np.all(np.isnan(O.e4m3_to_f64(np.array([0x7F, 0xFF]))))
+
+
+def test_e4m3_matches_torch_for_every_code():
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    ours = O.e4m3_to_f64(codes)
+    theirs = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    finite = ~np.isnan(ours)
+    assert finite.sum() == 254
+    np.testing.assert_array_equal(ours[finite], theirs[finite])
+    assert np.all(np.isnan(theirs[~finite]))
+
+
+def test_e4m3_positive_codes_strictly_increase():
+    v = O.e4m3_to_f64(np.arange(0, 127))
+    assert np.all(np.diff(v) > 0)
+
+
+def test_dequantize_rows_scales_each_output_channel():
+    codes = np.array([[0x38, 0x40], [0x30, 0xB8]], dtype=np.uint8)
+    np.testing.assert_array_equal(O.dequantize_rows(codes, [3.0, 0.25]),
+                                  [[3.0, 6.0], [0.125, -0.25]])
