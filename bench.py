@@ -43,6 +43,12 @@ WORKLOAD_TEXT = {
     "dsv3_prefill_noaux": "DeepSeek-V3-shaped MoE prefill layer with DeepSeek-V3's router "
                           "(T=8192, d=7168, E=256 top-8 ranked by sigmoid + selection bias, "
                           "8 groups / 4 kept, d_ff=2048, 1 shared expert, renorm x2.5, bf16)",
+    "dsv3_decode_fp8": "DeepSeek-V3-shaped decode layer with E4M3 expert weights (T=64, "
+                       "d=7168, E=256 top-8, d_ff=2048, 1 shared expert, sigmoid, renorm x2.5, "
+                       "bf16 activations, one fp32 scale per weight row)",
+    "dsv3_prefill_fp8": "DeepSeek-V3-shaped MoE prefill layer with E4M3 expert weights (T=8192, "
+                        "d=7168, E=256 top-8, d_ff=2048, 1 shared expert, sigmoid, renorm x2.5, "
+                        "bf16 activations, one fp32 scale per weight row)",
     "dsv3_decode": "DeepSeek-V3-shaped decode layer (T=64, d=7168, E=256 top-8, d_ff=2048, "
                    "1 shared expert, sigmoid, renorm x2.5, bf16)",
     "tiny": "tiny fp32 layer (T=64, d=128, E=4 top-2, d_ff=256)",
@@ -202,16 +208,19 @@ def algorithmic_work(shape, counts):
     kept = int(sum(counts))
     touched = int(sum(1 for c in counts if c > 0))
     eb = 2 if shape.dtype == "bf16" else 4
+    fp8 = getattr(shape, "weight_format", "act") == "fp8"
+    wb = 1 if fp8 else eb          # bytes per expert weight (E4M3 codes: 1)
+    sb = 4 if fp8 else 0           # bytes of the fp32 scale of one weight row
     fl_router = 2.0 * T * E * d
     fl_gate_up = 2.0 * kept * 2 * F * d + 2.0 * T * 2 * Fs * d
     fl_down = 2.0 * kept * F * d + 2.0 * T * Fs * d
-    w_bytes_touched = touched * 3 * d * F * eb + 3 * d * Fs * eb + E * d * eb
+    b_gate_up = touched * 2 * F * (d * wb + sb) + 2 * Fs * (d * wb + sb)
+    b_down = touched * d * (F * wb + sb) + d * (Fs * wb + sb)
     return {"kept": kept, "touched": touched, "flops_router": fl_router,
             "flops_gate_up": fl_gate_up, "flops_down": fl_down,
             "flops": fl_router + fl_gate_up + fl_down,
-            "bytes_gate_up": touched * 2 * d * F * eb + 2 * d * Fs * eb,
-            "bytes_down": touched * d * F * eb + d * Fs * eb,
-            "weight_bytes": w_bytes_touched}
+            "bytes_gate_up": b_gate_up, "bytes_down": b_down,
+            "weight_bytes": b_gate_up + b_down + E * d * eb}
 
 
 # ---------------------------------------------------------------------------
@@ -223,6 +232,7 @@ def time_oracle(shape, inputs, sample_tokens: int, steps: int, warmup: int = 0):
     of ``sample_tokens`` tokens per step.  Expert weights are widened to f64 once
     before timing (resident, as the GPU's weights are resident in HBM)."""
     import numpy as np
+    import torch
     from oracle import moe_oracle as O
     from workloads.generate import to_f64
 
@@ -230,11 +240,19 @@ def time_oracle(shape, inputs, sample_tokens: int, steps: int, warmup: int = 0):
     wr = to_f64(inputs["w_router"])
     bias = to_f64(inputs["router_bias"])
     E = shape.E
-    experts = [(to_f64(inputs["w_gate"][e]), to_f64(inputs["w_up"][e]),
-                to_f64(inputs["w_down"][e])) for e in range(E)]
+
+    def widen(key, e=None):
+        t = inputs[key] if e is None else inputs[key][e]
+        if inputs.get(key + "_scale") is None:
+            return to_f64(t)
+        s = inputs[key + "_scale"] if e is None else inputs[key + "_scale"][e]
+        codes = t.detach().contiguous().view(torch.uint8).cpu().numpy()
+        return O.dequantize_rows(codes, to_f64(s))
+
+    experts = [(widen("w_gate", e), widen("w_up", e), widen("w_down", e)) for e in range(E)]
     shared = None
     if inputs.get("ws_gate") is not None:
-        shared = (to_f64(inputs["ws_gate"]), to_f64(inputs["ws_up"]), to_f64(inputs["ws_down"]))
+        shared = (widen("ws_gate"), widen("ws_up"), widen("ws_down"))
     cap = O.expert_capacity(shape.T, shape.E, shape.capacity_factor)
     rng = np.random.default_rng(0)
     times = []
@@ -356,8 +374,8 @@ def main(argv=None):
     def step(evs):
         return moe.moe_layer_forward_profiled(cfg, x, w.w_router, w.router_bias, w.score_bias,
                                               w.w_gate, w.w_up, w.w_down, w.ws_gate, w.ws_up,
-                                              w.ws_down, w.shared_gate, y, topk_idx, topk_w,
-                                              counts, drops, mean_prob, ws, evs, stream)
+                                              w.ws_down, w.shared_gate, w.scales, y, topk_idx,
+                                              topk_w, counts, drops, mean_prob, ws, evs, stream)
 
     for _ in range(args.warmup):
         step(warm_events)

@@ -72,6 +72,15 @@ typedef enum {
 
 typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID = 1 } moe_gate_t;
 typedef enum { MOE_BF16 = 0, MOE_FP32 = 1 } moe_dtype_t;
+/* Storage of the routed and shared expert weights (the router weight is
+ * always act_dtype).  MOE_WEIGHTS_FP8_E4M3: each weight is an 8-bit E4M3 code
+ * (1 sign, 4 exponent bits of bias 7, 3 mantissa bits; max 448; NaN codes out
+ * of contract) times an fp32 scale of its output channel
+ * (moe_weight_scales_t) - "10. 混合专家 MoE", section "推理时": DeepSeek-V3
+ * ships FP8 weights, about one byte per parameter.  Requires act_dtype
+ * MOE_BF16; the products are exact in bf16 and the scale is applied to the
+ * fp32 accumulator of each output. */
+typedef enum { MOE_WEIGHTS_ACT = 0, MOE_WEIGHTS_FP8_E4M3 = 1 } moe_weight_format_t;
 
 /* Layer description.  All fields are plain 32-bit values. */
 typedef struct {
@@ -91,7 +100,20 @@ typedef struct {
                              Otherwise 2..32, dividing n_experts into groups of >= 2 */
   int32_t topk_group;     /* groups kept per token when n_group > 1 (1..n_group;
                              top_k <= topk_group * n_experts / n_group)           */
+  int32_t weight_format;  /* moe_weight_format_t of the expert weights          */
 } moe_config_t;
+
+/* Per-output-channel scales of E4M3 expert weights (weight_format ==
+ * MOE_WEIGHTS_FP8_E4M3): weight[row, c] = e4m3(code[row, c]) * scale[row].
+ * Device fp32 arrays, 16-byte aligned.  Pass NULL for MOE_WEIGHTS_ACT. */
+typedef struct {
+  const float* gate_scale;         /* [E, F] (rows of w_gate)                */
+  const float* up_scale;           /* [E, F] (rows of w_up)                  */
+  const float* down_scale;         /* [E, d] (rows of w_down)                */
+  const float* shared_gate_scale;  /* [F_s]; NULL without a shared expert    */
+  const float* shared_up_scale;    /* [F_s]                                   */
+  const float* shared_down_scale;  /* [d]                                     */
+} moe_weight_scales_t;
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 MOE_API int32_t moe_version(void);
@@ -214,7 +236,9 @@ MOE_API moe_status_t moe_dispatch_no_workspace(const moe_config_t* cfg, const in
  * the block sketch's per-expert loop).  Row r < offsets[E] of the grouped
  * batch is token perm[r] / k and belongs to the expert whose segment holds r:
  *   y_perm[r, :] = E_e(x[perm[r] / k, :])            fp32 [T * k, d]
- * Rows at and beyond offsets[E] are left unspecified.  If the shared expert
+ * Rows at and beyond offsets[E] are left unspecified.  Expert weights are
+ * act_dtype, or E4M3 codes with `scales` when cfg->weight_format is
+ * MOE_WEIGHTS_FP8_E4M3 (scales must be NULL otherwise).  If the shared expert
  * weights are given (cfg->d_ff_shared > 0), also
  *   y_shared[t, :] = S(x[t, :])                      fp32 [T, d]
  * ws_gate/ws_up/ws_down/y_shared must all be NULL when d_ff_shared == 0. */
@@ -222,6 +246,7 @@ MOE_API moe_status_t moe_grouped_swiglu(const moe_config_t* cfg, const void* x,
                                 const int32_t* perm, const int32_t* offsets,
                                 const void* w_gate, const void* w_up, const void* w_down,
                                 const void* ws_gate, const void* ws_up, const void* ws_down,
+                                const moe_weight_scales_t* scales,
                                 float* y_perm, float* y_shared,
                                 void* ws, size_t ws_bytes, void* stream);
 
@@ -267,13 +292,15 @@ MOE_API moe_status_t moe_balance_loss(const moe_config_t* cfg, const int32_t* co
  *   shared_gate [d] act_dtype or NULL: when given (requires the shared
  *     expert), the shared expert's output is scaled per token by
  *     sigmoid(x_t . shared_gate) (moe_shared_gate_weights);
+ *   scales: E4M3 weight scales (cfg->weight_format MOE_WEIGHTS_FP8_E4M3),
+ *     else NULL;
  *   topk_idx [T, k], topk_w [T, k], counts [E], drops [E], mean_prob [E]
  *     are optional outputs (NULL = not returned). */
 MOE_API moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const void* w_router,
                                const float* router_bias, const float* score_bias,
                                const void* w_gate, const void* w_up, const void* w_down,
                                const void* ws_gate, const void* ws_up, const void* ws_down,
-                               const void* shared_gate,
+                               const void* shared_gate, const moe_weight_scales_t* scales,
                                void* y, int32_t* topk_idx, float* topk_w,
                                int32_t* counts, int32_t* drops, float* mean_prob,
                                void* ws, size_t ws_bytes, void* stream);
@@ -300,7 +327,8 @@ MOE_API moe_status_t moe_layer_forward_profiled(
     const moe_config_t* cfg, const void* x, const void* w_router, const float* router_bias,
     const float* score_bias, const void* w_gate, const void* w_up, const void* w_down,
     const void* ws_gate, const void* ws_up, const void* ws_down, const void* shared_gate,
-    void* y, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* drops,
+    const moe_weight_scales_t* scales, void* y, int32_t* topk_idx, float* topk_w,
+    int32_t* counts, int32_t* drops,
     float* mean_prob, void* ws, size_t ws_bytes, void* stream,
     void** stage_events, int32_t* n_launches);
 

@@ -34,6 +34,21 @@ def assert_layer_close(y_gpu: np.ndarray, y_ref: np.ndarray, what: str = "y"):
     return mx / rms, mean / rms
 
 
+def assert_capacity_layer_close(y_gpu: np.ndarray, y_ref: np.ndarray, drop_mask: np.ndarray,
+                                what: str = "y"):
+    """With a capacity: tokens whose every choice was dropped must equal the
+    reference exactly (0, or the shared expert's output), and the others are
+    held to the layer tolerance relative to their own RMS (the dropped
+    tokens' exact zeros would otherwise deflate the RMS of the comparison)."""
+    y_gpu = np.asarray(y_gpu, dtype=np.float64)
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    all_dropped = np.all(np.asarray(drop_mask).reshape(y_ref.shape[0], -1) != 0, axis=1)
+    if all_dropped.any():
+        np.testing.assert_allclose(y_gpu[all_dropped], y_ref[all_dropped], rtol=2e-3, atol=1e-6)
+    if (~all_dropped).any():
+        assert_layer_close(y_gpu[~all_dropped], y_ref[~all_dropped], what)
+
+
 def score_margins(scores: np.ndarray, idx: np.ndarray) -> np.ndarray:
     """Per token: score of the k-th chosen expert minus the best unchosen score
     (inf when every expert is chosen)."""
@@ -70,15 +85,50 @@ def oracle_capacity(shape, T: Optional[int] = None) -> Optional[int]:
     return O.expert_capacity(T, shape.E, shape.capacity_factor)
 
 
+def _codes(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().view(torch.uint8).cpu().numpy()
+
+
+class DequantExperts:
+    """Per-expert float64 weights of an E4M3 layer: the oracle's decoding of
+    the stored codes times the per-row scales, one expert at a time."""
+
+    def __init__(self, inputs):
+        self.q = (inputs["w_gate"], inputs["w_up"], inputs["w_down"])
+        self.s = (inputs["w_gate_scale"], inputs["w_up_scale"], inputs["w_down_scale"])
+
+    def __len__(self) -> int:
+        return self.q[0].shape[0]
+
+    def __getitem__(self, e: int):
+        return tuple(O.dequantize_rows(_codes(q[e]), to_f64(s[e])) for q, s in zip(self.q, self.s))
+
+
+def layer_experts(inputs):
+    """The routed experts as float64 weights (exact widening, or E4M3 decoding)."""
+    if inputs.get("w_gate_scale") is not None:
+        return DequantExperts(inputs)
+    return ExpertWeights(inputs["w_gate"], inputs["w_up"], inputs["w_down"])
+
+
+def layer_shared(inputs):
+    if inputs.get("ws_gate") is None:
+        return None
+    if inputs.get("ws_gate_scale") is not None:
+        return tuple(O.dequantize_rows(_codes(inputs[k]), to_f64(inputs[k + "_scale"]))
+                     for k in ("ws_gate", "ws_up", "ws_down"))
+    return shared_weights(inputs)
+
+
 def oracle_layer(shape, inputs, tokens: Optional[Sequence[int]] = None):
-    """Run the float64 oracle on the (bf16/fp32) inputs, widened exactly."""
+    """Run the float64 oracle on the (bf16/fp32/E4M3) inputs, widened exactly."""
     T = inputs["x"].shape[0]
     return O.moe_layer_forward(
         to_f64(inputs["x"]), to_f64(inputs["w_router"]),
-        ExpertWeights(inputs["w_gate"], inputs["w_up"], inputs["w_down"]),
+        layer_experts(inputs),
         k=shape.k, gate=shape.gate, renormalize=shape.renormalize,
         routed_scaling_factor=shape.rsf, capacity=oracle_capacity(shape, T),
-        router_bias=to_f64(inputs["router_bias"]), shared=shared_weights(inputs),
+        router_bias=to_f64(inputs["router_bias"]), shared=layer_shared(inputs),
         tokens=tokens, score_bias=to_f64(inputs.get("score_bias")),
         n_group=max(shape.n_group, 1), topk_group=shape.topk_group,
         shared_gate=to_f64(inputs.get("shared_gate")))

@@ -132,21 +132,36 @@ def test_entry_points_reject_missing_workspace_and_pointers():
                             None) == B.MOE_ERR_INVALID_ARG
     # layer: shared weights given although d_ff_shared == 0
     assert lib.moe_layer_forward(ctypes.byref(cfg), fake, fake, None, None, fake, fake, fake, fake,
-                                 fake, fake, None, fake, None, None, None, None, None, fake, need,
-                                 None) == B.MOE_ERR_INVALID_ARG
+                                 fake, fake, None, None, fake, None, None, None, None, None, fake,
+                                 need, None) == B.MOE_ERR_INVALID_ARG
     # layer: only some shared weights
     cs = _cfg(F_s=128)
     _, need_s = _ws_size(cs)
     assert lib.moe_layer_forward(ctypes.byref(cs), fake, fake, None, None, fake, fake, fake, fake,
-                                 None, fake, None, fake, None, None, None, None, None, fake,
+                                 None, fake, None, None, fake, None, None, None, None, None, fake,
                                  need_s, None) == B.MOE_ERR_INVALID_ARG
     # layer: a shared-expert gate without a shared expert
     assert lib.moe_layer_forward(ctypes.byref(cfg), fake, fake, None, None, fake, fake, fake,
-                                 None, None, None, fake, fake, None, None, None, None, None,
+                                 None, None, None, fake, None, fake, None, None, None, None, None,
                                  fake, need, None) == B.MOE_ERR_INVALID_ARG
+    # E4M3 weights: scales required, and only with bf16 activations
+    c8 = _cfg(act_dtype="bf16", weight_format="fp8")
+    _, need8 = _ws_size(c8)
+    assert lib.moe_layer_forward(ctypes.byref(c8), fake, fake, None, None, fake, fake, fake,
+                                 None, None, None, None, None, fake, None, None, None, None, None,
+                                 fake, need8, None) == B.MOE_ERR_INVALID_ARG
+    sc = B.MoEWeightScales(fake, fake, fake + 4, None, None, None)   # misaligned down scales
+    assert lib.moe_layer_forward(ctypes.byref(c8), fake, fake, None, None, fake, fake, fake,
+                                 None, None, None, None, ctypes.byref(sc), fake, None, None, None,
+                                 None, None, fake, need8, None) == B.MOE_ERR_INVALID_ARG
+    sc_ok = B.MoEWeightScales(fake, fake, fake, None, None, None)
+    assert lib.moe_layer_forward(ctypes.byref(cfg), fake, fake, None, None, fake, fake, fake,
+                                 None, None, None, None, ctypes.byref(sc_ok), fake, None, None,
+                                 None, None, None, fake, need, None) == B.MOE_ERR_INVALID_ARG
+    assert _ws_size(_cfg(act_dtype="fp32", weight_format="fp8"))[0] == B.MOE_ERR_UNSUPPORTED
     # null config
     assert lib.moe_layer_forward(None, fake, fake, None, None, fake, fake, fake, None, None, None,
-                                 None, fake, None, None, None, None, None, fake, need,
+                                 None, None, fake, None, None, None, None, None, fake, need,
                                  None) == B.MOE_ERR_INVALID_ARG
     # balance loss / shared gate: null outputs
     assert lib.moe_balance_loss(ctypes.byref(cfg), fake, None, fake, 0.01, None,

@@ -16,8 +16,8 @@ from oracle import moe_oracle as O
 from workloads import SHAPES, MoEShape, make_inputs
 from workloads.generate import to_f64
 
-from gpu_util import (MARGIN, assert_layer_close, np_f, np_i, oracle_layer, same_sets,
-                      score_margins)
+from gpu_util import (MARGIN, assert_capacity_layer_close, assert_layer_close, np_f, np_i,
+                      oracle_layer, same_sets, score_margins)
 
 pytestmark = pytest.mark.gpu
 
@@ -80,7 +80,7 @@ def test_layer_matches_oracle_all_tokens(name, layout, monkeypatch):
         if same.all():
             np.testing.assert_array_equal(np_i(out["counts"]), ref["counts"])
             np.testing.assert_array_equal(np_i(out["drops"]), ref["drops"])
-            assert_layer_close(np_f(out["y"]), ref["y"], name)
+            assert_capacity_layer_close(np_f(out["y"]), ref["y"], ref["drop_mask"], name)
     # statistics
     if same.all():
         np.testing.assert_array_equal(np_i(out["counts"]) + np_i(out["drops"]),

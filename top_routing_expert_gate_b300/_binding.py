@@ -28,6 +28,8 @@ MOE_GATE_SOFTMAX = 0
 MOE_GATE_SIGMOID = 1
 MOE_BF16 = 0
 MOE_FP32 = 1
+MOE_WEIGHTS_ACT = 0
+MOE_WEIGHTS_FP8_E4M3 = 1
 
 
 class MoEConfig(ctypes.Structure):
@@ -47,13 +49,27 @@ class MoEConfig(ctypes.Structure):
         ("out_dtype", c_int32),
         ("n_group", c_int32),
         ("topk_group", c_int32),
+        ("weight_format", c_int32),
     ]
 
     def __repr__(self):
         return "MoEConfig(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
 
 
+class MoEWeightScales(ctypes.Structure):
+    """Mirror of moe_weight_scales_t (device pointers)."""
+    _fields_ = [
+        ("gate_scale", c_void_p),
+        ("up_scale", c_void_p),
+        ("down_scale", c_void_p),
+        ("shared_gate_scale", c_void_p),
+        ("shared_up_scale", c_void_p),
+        ("shared_down_scale", c_void_p),
+    ]
+
+
 CFG = POINTER(MoEConfig)
+SCALES = POINTER(MoEWeightScales)
 _I32P = c_void_p   # device pointers are passed as plain addresses
 
 # name -> (restype, argtypes); every function of include/moe_b300.h
@@ -73,7 +89,7 @@ SIGNATURES = {
     "moe_dispatch_no_workspace": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p,
                                             c_void_p, c_void_p, c_void_p]),
     "moe_grouped_swiglu": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                     c_void_p, c_void_p, c_void_p, c_void_p, SCALES, c_void_p,
                                      c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_combine": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                               c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
@@ -82,13 +98,13 @@ SIGNATURES = {
                                    c_void_p]),
     "moe_layer_forward": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                    c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                    c_void_p, SCALES, c_void_p, c_void_p, c_void_p, c_void_p,
                                     c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_layer_forward_profiled": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p,
                                              c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                             c_void_p, c_void_p, SCALES, c_void_p, c_void_p,
                                              c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                             c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
-                                             c_void_p, c_void_p, c_void_p]),
+                                             c_size_t, c_void_p, c_void_p, c_void_p]),
     "moe_get_error": (c_int32, [c_void_p, c_void_p]),
     "moe_selftest_bounded_wait": (c_int32, [c_void_p, c_size_t, ctypes.c_uint64, c_void_p]),
 }

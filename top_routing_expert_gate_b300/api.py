@@ -22,15 +22,19 @@ _DT = {"bf16": B.MOE_BF16, "fp32": B.MOE_FP32}
 _TORCH_DT = {B.MOE_BF16: torch.bfloat16, B.MOE_FP32: torch.float32}
 
 
+_WF = {"act": B.MOE_WEIGHTS_ACT, "fp8": B.MOE_WEIGHTS_FP8_E4M3}
+
+
 def make_config(T: int, d: int, E: int, k: int, F: int, F_s: int = 0, gate: str = "softmax",
                 renormalize: bool = True, rsf: float = 1.0, capacity: int = -1,
                 act_dtype: str = "bf16", out_dtype: str = "fp32", n_group: int = 0,
-                topk_group: int = 0) -> MoEConfig:
+                topk_group: int = 0, weight_format: str = "act") -> MoEConfig:
     return MoEConfig(T=T, d_model=d, n_experts=E, top_k=k, d_ff=F, d_ff_shared=F_s,
                      gate=B.MOE_GATE_SOFTMAX if gate == "softmax" else B.MOE_GATE_SIGMOID,
                      renormalize=1 if renormalize else 0, routed_scaling_factor=float(rsf),
                      capacity=int(capacity), act_dtype=_DT[act_dtype], out_dtype=_DT[out_dtype],
-                     n_group=int(n_group), topk_group=int(topk_group))
+                     n_group=int(n_group), topk_group=int(topk_group),
+                     weight_format=_WF[weight_format])
 
 
 def config_from_shape(shape, out_dtype: str = "fp32", T: Optional[int] = None) -> MoEConfig:
@@ -41,7 +45,8 @@ def config_from_shape(shape, out_dtype: str = "fp32", T: Optional[int] = None) -
         cap = moe_capacity(T, shape.E, shape.capacity_factor)
     return make_config(T, shape.d, shape.E, shape.k, shape.F, shape.F_s, shape.gate,
                        shape.renormalize, shape.rsf, cap, shape.dtype, out_dtype,
-                       getattr(shape, "n_group", 0), getattr(shape, "topk_group", 0))
+                       getattr(shape, "n_group", 0), getattr(shape, "topk_group", 0),
+                       getattr(shape, "weight_format", "act"))
 
 
 def act_dtype(cfg: MoEConfig) -> torch.dtype:
@@ -130,12 +135,42 @@ def moe_dispatch(cfg, topk_idx, counts, drops, offsets, perm, drop_mask, ws: Wor
         _ptr(perm), _ptr(drop_mask), ws.ptr, ws.nbytes, _stream(stream)), "moe_dispatch")
 
 
+@dataclass
+class WeightScales:
+    """Per-output-channel fp32 scales of E4M3 expert weights (moe_weight_scales_t)."""
+    gate: torch.Tensor                 # [E, F]
+    up: torch.Tensor                   # [E, F]
+    down: torch.Tensor                 # [E, d]
+    shared_gate: Optional[torch.Tensor] = None   # [F_s]
+    shared_up: Optional[torch.Tensor] = None     # [F_s]
+    shared_down: Optional[torch.Tensor] = None   # [d]
+
+    def as_c(self) -> B.MoEWeightScales:
+        return B.MoEWeightScales(_ptr(self.gate, "gate scale"), _ptr(self.up, "up scale"),
+                                 _ptr(self.down, "down scale"), _ptr(self.shared_gate),
+                                 _ptr(self.shared_up), _ptr(self.shared_down))
+
+    @classmethod
+    def from_inputs(cls, inputs) -> Optional["WeightScales"]:
+        if inputs.get("w_gate_scale") is None:
+            return None
+        return cls(inputs["w_gate_scale"], inputs["w_up_scale"], inputs["w_down_scale"],
+                   inputs.get("ws_gate_scale"), inputs.get("ws_up_scale"),
+                   inputs.get("ws_down_scale"))
+
+
+def _scales_ref(scales: Optional[WeightScales]):
+    return None if scales is None else ctypes.byref(scales.as_c())
+
+
 def moe_grouped_swiglu(cfg, x, perm, offsets, w_gate, w_up, w_down, ws_gate, ws_up, ws_down,
-                       y_perm, y_shared, ws: Workspace, stream=None) -> None:
+                       y_perm, y_shared, ws: Workspace, stream=None,
+                       scales: Optional[WeightScales] = None) -> None:
     check(load_library().moe_grouped_swiglu(
         ctypes.byref(cfg), _ptr(x), _ptr(perm), _ptr(offsets), _ptr(w_gate), _ptr(w_up),
-        _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), _ptr(y_perm), _ptr(y_shared),
-        ws.ptr, ws.nbytes, _stream(stream)), "moe_grouped_swiglu")
+        _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), _scales_ref(scales),
+        _ptr(y_perm), _ptr(y_shared), ws.ptr, ws.nbytes, _stream(stream)),
+        "moe_grouped_swiglu")
 
 
 def moe_combine(cfg, y_perm, topk_w, offsets, perm, drop_mask, y_shared, shared_weight, y,
@@ -159,19 +194,19 @@ def moe_balance_loss(cfg, counts, drops, mean_prob, alpha: float, loss, stream=N
 
 
 def moe_layer_forward(cfg, x, w_router, router_bias, score_bias, w_gate, w_up, w_down, ws_gate,
-                      ws_up, ws_down, shared_gate, y, topk_idx, topk_w, counts, drops, mean_prob,
-                      ws: Workspace, stream=None) -> None:
+                      ws_up, ws_down, shared_gate, scales, y, topk_idx, topk_w, counts, drops,
+                      mean_prob, ws: Workspace, stream=None) -> None:
     check(load_library().moe_layer_forward(
         ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(score_bias),
         _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down),
-        _ptr(shared_gate), _ptr(y),
+        _ptr(shared_gate), _scales_ref(scales), _ptr(y),
         _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(drops), _ptr(mean_prob), ws.ptr,
         ws.nbytes, _stream(stream)), "moe_layer_forward")
 
 
 def moe_layer_forward_profiled(cfg, x, w_router, router_bias, score_bias, w_gate, w_up, w_down,
-                               ws_gate, ws_up, ws_down, shared_gate, y, topk_idx, topk_w, counts,
-                               drops, mean_prob, ws: Workspace, stage_events,
+                               ws_gate, ws_up, ws_down, shared_gate, scales, y, topk_idx, topk_w,
+                               counts, drops, mean_prob, ws: Workspace, stage_events,
                                stream=None) -> int:
     """moe_layer_forward recording ``stage_events`` (MOE_NUM_STAGES + 1
     torch.cuda.Event with timing, already recorded once so that they exist)
@@ -183,9 +218,10 @@ def moe_layer_forward_profiled(cfg, x, w_router, router_bias, score_bias, w_gate
     check(load_library().moe_layer_forward_profiled(
         ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(score_bias),
         _ptr(w_gate),
-        _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), _ptr(shared_gate), _ptr(y),
-        _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(drops), _ptr(mean_prob), ws.ptr,
-        ws.nbytes, _stream(stream), arr, ctypes.byref(n)), "moe_layer_forward_profiled")
+        _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), _ptr(shared_gate),
+        _scales_ref(scales), _ptr(y), _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(drops),
+        _ptr(mean_prob), ws.ptr, ws.nbytes, _stream(stream), arr, ctypes.byref(n)),
+        "moe_layer_forward_profiled")
     return n.value
 
 
@@ -255,12 +291,14 @@ class LayerWeights:
     ws_down: Optional[torch.Tensor] = None
     score_bias: Optional[torch.Tensor] = None
     shared_gate: Optional[torch.Tensor] = None
+    scales: Optional[WeightScales] = None     # E4M3 expert weights only
 
     @classmethod
     def from_inputs(cls, inputs) -> "LayerWeights":
         return cls(inputs["w_router"], inputs["w_gate"], inputs["w_up"], inputs["w_down"],
                    inputs.get("router_bias"), inputs.get("ws_gate"), inputs.get("ws_up"),
-                   inputs.get("ws_down"), inputs.get("score_bias"), inputs.get("shared_gate"))
+                   inputs.get("ws_down"), inputs.get("score_bias"), inputs.get("shared_gate"),
+                   WeightScales.from_inputs(inputs))
 
 
 def layer_forward(cfg, x, w: LayerWeights, ws: Optional[Workspace] = None,
@@ -275,7 +313,7 @@ def layer_forward(cfg, x, w: LayerWeights, ws: Optional[Workspace] = None,
                    drops=_i32(E, dev), mean_prob=_f32(E, dev))
     g = out.get
     moe_layer_forward(cfg, x, w.w_router, w.router_bias, w.score_bias, w.w_gate, w.w_up,
-                      w.w_down, w.ws_gate, w.ws_up, w.ws_down, w.shared_gate, out["y"],
+                      w.w_down, w.ws_gate, w.ws_up, w.ws_down, w.shared_gate, w.scales, out["y"],
                       g("topk_idx"),
                       g("topk_w"), g("counts"), g("drops"), g("mean_prob"), ws, stream)
     return out

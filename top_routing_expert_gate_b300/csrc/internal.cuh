@@ -163,6 +163,7 @@ struct ExpertArgs {
   float* y_perm;        // [A, d]
   float* y_shared;      // [T, d]
   int32_t* status;
+  const moe_weight_scales_t* scales = nullptr;   // E4M3 weights only
   cudaEvent_t ev_up = nullptr;     // recorded before the gate/up GEMM when set (fp32 path)
   cudaEvent_t ev_down = nullptr;   // recorded before the down GEMM when set (fp32 path)
   LaunchCounter* launches = nullptr;
@@ -178,5 +179,8 @@ constexpr int kGemmGateUp = 0;
 constexpr int kGemmDown = 1;
 cudaError_t launch_gemm_tc(const moe_config_t& c, const ExpertArgs& a, int which, cudaStream_t s);
 cudaError_t launch_gemm_wm(const moe_config_t& c, const ExpertArgs& a, int which, cudaStream_t s);
+// Tokens in M with E4M3 expert weights widened to bf16 on chip (a.scales set).
+cudaError_t launch_gemm_fp8w(const moe_config_t& c, const ExpertArgs& a, int which,
+                             cudaStream_t s);
 
 }  // namespace moe

@@ -79,6 +79,10 @@ moe_status_t check_config(const moe_config_t* c) {
     if (c->d_model % 64 != 0 || c->d_ff % 128 != 0 || c->d_ff_shared % 128 != 0)
       return MOE_ERR_UNSUPPORTED;
   }
+  if (c->weight_format != MOE_WEIGHTS_ACT && c->weight_format != MOE_WEIGHTS_FP8_E4M3)
+    return MOE_ERR_INVALID_ARG;
+  if (c->weight_format == MOE_WEIGHTS_FP8_E4M3 && c->act_dtype != MOE_BF16)
+    return MOE_ERR_UNSUPPORTED;
   // expert groups: 0 or 1 = none; otherwise equal groups of at least two
   // experts, at most 32 groups (one warp lane scores each group)
   if (c->n_group < 0) return MOE_ERR_INVALID_ARG;
@@ -137,17 +141,32 @@ bool weights_in_m(const moe_config_t& c, int which) {
 
 cudaError_t run_experts(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s) {
   if (c.act_dtype != MOE_BF16) return launch_experts_simt(c, a, s);
+  const bool fp8 = c.weight_format == MOE_WEIGHTS_FP8_E4M3;
   for (int which = kGemmGateUp; which <= kGemmDown; ++which) {
     cudaEvent_t ev = which == kGemmGateUp ? a.ev_up : a.ev_down;
     if (ev) {
       const cudaError_t e = cudaEventRecord(ev, s);
       if (e != cudaSuccess) return e;
     }
-    const cudaError_t e = weights_in_m(c, which) ? launch_gemm_wm(c, a, which, s)
-                                                 : launch_gemm_tc(c, a, which, s);
+    const cudaError_t e = fp8                     ? launch_gemm_fp8w(c, a, which, s)
+                          : weights_in_m(c, which) ? launch_gemm_wm(c, a, which, s)
+                                                   : launch_gemm_tc(c, a, which, s);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+// E4M3 weights need every scale array of the weights in use; other formats none.
+moe_status_t check_scales(const moe_config_t* c, const moe_weight_scales_t* sc,
+                          bool has_shared) {
+  if (c->weight_format != MOE_WEIGHTS_FP8_E4M3) return sc ? MOE_ERR_INVALID_ARG : MOE_OK;
+  if (!sc) return MOE_ERR_INVALID_ARG;
+  auto bad = [](const float* p) { return p == nullptr || !aligned16(p); };
+  if (bad(sc->gate_scale) || bad(sc->up_scale) || bad(sc->down_scale)) return MOE_ERR_INVALID_ARG;
+  if (has_shared && (bad(sc->shared_gate_scale) || bad(sc->shared_up_scale) ||
+                     bad(sc->shared_down_scale)))
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
 }
 
 moe_status_t check_shared_args(const moe_config_t* c, const void* g, const void* u,
@@ -165,7 +184,7 @@ moe_status_t check_shared_args(const moe_config_t* c, const void* g, const void*
 
 extern "C" {
 
-int32_t moe_version(void) { return 200; }
+int32_t moe_version(void) { return 300; }
 
 const char* moe_status_string(moe_status_t st) {
   switch (st) {
@@ -265,8 +284,9 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* topk_idx, int3
 moe_status_t moe_grouped_swiglu(const moe_config_t* cfg, const void* x, const int32_t* perm,
                                 const int32_t* offsets, const void* w_gate, const void* w_up,
                                 const void* w_down, const void* ws_gate, const void* ws_up,
-                                const void* ws_down, float* y_perm, float* y_shared, void* ws,
-                                size_t ws_bytes, void* stream) {
+                                const void* ws_down, const moe_weight_scales_t* scales,
+                                float* y_perm, float* y_shared, void* ws, size_t ws_bytes,
+                                void* stream) {
   MOE_TRY(check_config(cfg));
   MOE_TRY(check_ws(cfg, ws, ws_bytes));
   if (bad_ptr(cfg, x) || bad_ptr(cfg, perm) || bad_ptr(cfg, w_gate) || bad_ptr(cfg, w_up) ||
@@ -275,6 +295,7 @@ moe_status_t moe_grouped_swiglu(const moe_config_t* cfg, const void* x, const in
   MOE_TRY(check_shared_args(cfg, ws_gate, ws_up, ws_down));
   if ((ws_gate != nullptr) != (y_shared != nullptr) || bad_opt(y_shared))
     return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_scales(cfg, scales, ws_gate != nullptr));
   if (cfg->T == 0) return MOE_OK;
   const WsLayout L = ws_layout(*cfg);
   cudaStream_t s = (cudaStream_t)stream;
@@ -296,6 +317,7 @@ moe_status_t moe_grouped_swiglu(const moe_config_t* cfg, const void* x, const in
   a.y_perm = y_perm;
   a.y_shared = y_shared;
   a.status = status;
+  a.scales = scales;
   return cuda_status(run_experts(*cfg, a, s));
 }
 
@@ -349,7 +371,8 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
                                 const float* router_bias, const float* score_bias,
                                 const void* w_gate, const void* w_up,
                                 const void* w_down, const void* ws_gate, const void* ws_up,
-                                const void* ws_down, const void* shared_gate, void* y,
+                                const void* ws_down, const void* shared_gate,
+                                const moe_weight_scales_t* scales, void* y,
                                 int32_t* topk_idx, float* topk_w, int32_t* counts,
                                 int32_t* drops, float* mean_prob, void* ws, size_t ws_bytes,
                                 void* stream, cudaEvent_t* ev, int32_t* n_launches) {
@@ -363,6 +386,7 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
     return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_shared_args(cfg, ws_gate, ws_up, ws_down));
   if (bad_opt(shared_gate) || (shared_gate && !ws_gate)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_scales(cfg, scales, ws_gate != nullptr));
   const WsLayout L = ws_layout(*cfg);
   cudaStream_t s = (cudaStream_t)stream;
   const moe_config_t& c = *cfg;
@@ -420,6 +444,7 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
   a.y_perm = at<float>(ws, L.y_perm);
   a.y_shared = has_shared ? at<float>(ws, L.y_shared) : nullptr;
   a.status = status;
+  a.scales = scales;
   a.ev_up = ev ? ev[MOE_STAGE_GATE_UP] : nullptr;
   a.ev_down = ev ? ev[MOE_STAGE_DOWN] : nullptr;
   a.launches = &lc;
@@ -440,13 +465,14 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
                                const float* router_bias, const float* score_bias,
                                const void* w_gate, const void* w_up,
                                const void* w_down, const void* ws_gate, const void* ws_up,
-                               const void* ws_down, const void* shared_gate, void* y,
+                               const void* ws_down, const void* shared_gate,
+                               const moe_weight_scales_t* scales, void* y,
                                int32_t* topk_idx, float* topk_w, int32_t* counts,
                                int32_t* drops, float* mean_prob, void* ws, size_t ws_bytes,
                                void* stream) {
   return layer_forward_impl(cfg, x, w_router, router_bias, score_bias, w_gate, w_up, w_down,
-                            ws_gate, ws_up, ws_down, shared_gate, y, topk_idx, topk_w, counts,
-                            drops, mean_prob, ws, ws_bytes, stream, nullptr, nullptr);
+                            ws_gate, ws_up, ws_down, shared_gate, scales, y, topk_idx, topk_w,
+                            counts, drops, mean_prob, ws, ws_bytes, stream, nullptr, nullptr);
 }
 
 moe_status_t moe_layer_forward_profiled(const moe_config_t* cfg, const void* x,
@@ -454,7 +480,8 @@ moe_status_t moe_layer_forward_profiled(const moe_config_t* cfg, const void* x,
                                         const float* score_bias, const void* w_gate,
                                         const void* w_up, const void* w_down,
                                         const void* ws_gate, const void* ws_up,
-                                        const void* ws_down, const void* shared_gate, void* y,
+                                        const void* ws_down, const void* shared_gate,
+                                        const moe_weight_scales_t* scales, void* y,
                                         int32_t* topk_idx, float* topk_w, int32_t* counts,
                                         int32_t* drops, float* mean_prob, void* ws,
                                         size_t ws_bytes, void* stream, void** stage_events,
@@ -463,9 +490,9 @@ moe_status_t moe_layer_forward_profiled(const moe_config_t* cfg, const void* x,
   for (int i = 0; i <= MOE_NUM_STAGES; ++i)
     if (!stage_events[i]) return MOE_ERR_INVALID_ARG;
   return layer_forward_impl(cfg, x, w_router, router_bias, score_bias, w_gate, w_up, w_down,
-                            ws_gate, ws_up, ws_down, shared_gate, y, topk_idx, topk_w, counts,
-                            drops, mean_prob, ws, ws_bytes, stream, (cudaEvent_t*)stage_events,
-                            n_launches);
+                            ws_gate, ws_up, ws_down, shared_gate, scales, y, topk_idx, topk_w,
+                            counts, drops, mean_prob, ws, ws_bytes, stream,
+                            (cudaEvent_t*)stage_events, n_launches);
 }
 
 moe_status_t moe_get_error(const void* ws, void* stream) {

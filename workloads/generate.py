@@ -16,6 +16,10 @@ Recipe (one torch.Generator stream per tensor, seeded from the tensor's name):
 * score_bias (shapes with score_bias_std): ~ N(0, std^2) [E] fp32, standing in
   for a selection-only bias after some training steps of +-gamma.
 * shared_gate (shapes with a gated shared expert) ~ N(0, 1/d) [d].
+* FP8 shapes: each expert weight above is drawn the same way in float32 and
+  stored as E4M3 codes (torch.float8_e4m3fn, round to nearest even) of
+  w / s with s = max|w_row| / 448 per output row, plus the fp32 row scales
+  (w_gate_scale, w_up_scale, w_down_scale, ws_*_scale).
 
 Values are drawn in float32 and then cast to the shape's dtype (bf16 or fp32).
 This module holds no routing or expert arithmetic.
@@ -50,6 +54,26 @@ def _normal(shape, std: float, name: str, seed_base: int, device, dtype) -> torc
     return t.to(dtype)
 
 
+E4M3_MAX = 448.0
+
+
+def quantize_rows_e4m3(w: torch.Tensor):
+    """(codes, scales): E4M3 codes of w / s and the per-row scales
+    s = max|w_row| / 448 (1 for an all-zero row)."""
+    w = w.float()
+    s = w.abs().amax(dim=-1) / E4M3_MAX
+    s = torch.where(s > 0, s, torch.ones_like(s))
+    q = (w / s.unsqueeze(-1)).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    return q, s
+
+
+def _weight(shape_, std, name, seed, device, dt, fp8: bool):
+    w = _normal(shape_, std, name, seed, device, torch.float32)
+    if fp8:
+        return quantize_rows_e4m3(w)
+    return w.to(dt), None
+
+
 def make_inputs(shape: MoEShape, device="cpu", seed: int = 0,
                 with_experts: bool = True) -> Dict[str, Optional[torch.Tensor]]:
     """All tensors of one layer instance, on ``device``.
@@ -73,18 +97,39 @@ def make_inputs(shape: MoEShape, device="cpu", seed: int = 0,
     else:
         out["score_bias"] = None
     if with_experts:
-        wg = torch.empty((E, F, d), dtype=dt, device=device)
-        wu = torch.empty((E, F, d), dtype=dt, device=device)
-        wd = torch.empty((E, d, F), dtype=dt, device=device)
+        fp8 = getattr(shape, "weight_format", "act") == "fp8"
+        wdt = torch.float8_e4m3fn if fp8 else dt
+        wg = torch.empty((E, F, d), dtype=wdt, device=device)
+        wu = torch.empty((E, F, d), dtype=wdt, device=device)
+        wd = torch.empty((E, d, F), dtype=wdt, device=device)
+        if fp8:
+            sg = torch.empty((E, F), dtype=torch.float32, device=device)
+            su = torch.empty((E, F), dtype=torch.float32, device=device)
+            sd = torch.empty((E, d), dtype=torch.float32, device=device)
         for e in range(E):
-            wg[e] = _normal((F, d), 1.0 / math.sqrt(d), f"w_gate.{e}", seed, device, dt)
-            wu[e] = _normal((F, d), 1.0 / math.sqrt(d), f"w_up.{e}", seed, device, dt)
-            wd[e] = _normal((d, F), 1.0 / math.sqrt(F), f"w_down.{e}", seed, device, dt)
+            q, s = _weight((F, d), 1.0 / math.sqrt(d), f"w_gate.{e}", seed, device, dt, fp8)
+            wg[e] = q
+            if fp8:
+                sg[e] = s
+            q, s = _weight((F, d), 1.0 / math.sqrt(d), f"w_up.{e}", seed, device, dt, fp8)
+            wu[e] = q
+            if fp8:
+                su[e] = s
+            q, s = _weight((d, F), 1.0 / math.sqrt(F), f"w_down.{e}", seed, device, dt, fp8)
+            wd[e] = q
+            if fp8:
+                sd[e] = s
         out["w_gate"], out["w_up"], out["w_down"] = wg, wu, wd
+        if fp8:
+            out["w_gate_scale"], out["w_up_scale"], out["w_down_scale"] = sg, su, sd
         if Fs > 0:
-            out["ws_gate"] = _normal((Fs, d), 1.0 / math.sqrt(d), "ws_gate", seed, device, dt)
-            out["ws_up"] = _normal((Fs, d), 1.0 / math.sqrt(d), "ws_up", seed, device, dt)
-            out["ws_down"] = _normal((d, Fs), 1.0 / math.sqrt(Fs), "ws_down", seed, device, dt)
+            for key, shp, std in (("ws_gate", (Fs, d), 1.0 / math.sqrt(d)),
+                                  ("ws_up", (Fs, d), 1.0 / math.sqrt(d)),
+                                  ("ws_down", (d, Fs), 1.0 / math.sqrt(Fs))):
+                q, s = _weight(shp, std, key, seed, device, dt, fp8)
+                out[key] = q
+                if fp8:
+                    out[key + "_scale"] = s
         else:
             out["ws_gate"] = out["ws_up"] = out["ws_down"] = None
         out["shared_gate"] = None

@@ -14,6 +14,9 @@ Each shape follows a model configuration that the pages describe:
 * ``dsv3_prefill_noaux`` - the same layer routed the way DeepSeek-V3 routes:
   ranking by sigmoid score plus a selection-only bias, with 8 expert groups of
   which each token may use 4 (same page, "DeepSeek-V3 的无辅助损失偏置").
+* ``dsv3_decode_fp8`` / ``dsv3_prefill_fp8`` - the DeepSeek-V3 layers with the
+  expert weights stored as FP8 E4M3 codes and one scale per output channel
+  (same page, "推理时": DeepSeek-V3 ships FP8 weights).
 * ``switch`` - a Switch-Transformer-style top-1 layer with an expert capacity
   of ceil(T/E x 1.25) and token dropping (same page, section
   "负载不均：路由坍缩与丢 token"), with a Zipf-skewed router bias so that the
@@ -47,6 +50,7 @@ class MoEShape:
     topk_group: int = 0               # groups kept per token
     score_bias_std: Optional[float] = None   # selection-only score bias ~ N(0, std^2)
     shared_gate: bool = False         # per-token sigmoid gate on the shared expert
+    weight_format: str = "act"        # "act" (weights in dtype) or "fp8" (E4M3 + row scales)
 
     def with_tokens(self, T: int) -> "MoEShape":
         return replace(self, T=T)
@@ -78,6 +82,15 @@ SHAPES = {
     "dsv3_decode": MoEShape("dsv3_decode", T=64, d=7168, E=256, k=8, F=2048,
                             F_s=2048, gate="sigmoid", renormalize=True, rsf=2.5,
                             capacity_factor=None, zipf_s=None, dtype="bf16"),
+    # the same layers with E4M3 expert weights (one scale per output channel)
+    "dsv3_decode_fp8": MoEShape("dsv3_decode_fp8", T=64, d=7168, E=256, k=8, F=2048,
+                                F_s=2048, gate="sigmoid", renormalize=True, rsf=2.5,
+                                capacity_factor=None, zipf_s=None, dtype="bf16",
+                                weight_format="fp8"),
+    "dsv3_prefill_fp8": MoEShape("dsv3_prefill_fp8", T=8192, d=7168, E=256, k=8, F=2048,
+                                 F_s=2048, gate="sigmoid", renormalize=True, rsf=2.5,
+                                 capacity_factor=None, zipf_s=None, dtype="bf16",
+                                 weight_format="fp8"),
 }
 
 
