@@ -14,15 +14,19 @@
 // applied once per output in the epilogue.
 //
 // Same tile layout as experts_tc.cu (tokens in the MMA's M, 128-row token
-// tiles, 256 weight rows per tile), with the weight operand widened on chip:
+// tiles, 256 weight rows per tile), with the weight operand widened on chip.
+// Three rings: E4M3 weight tiles (5 slots), bf16 token tiles (3 slots) and
+// widened bf16 weight tiles (2 slots):
 //   warp 0      TMA producer of the E4M3 weight tiles (256 rows x 64 bytes,
-//               unswizzled) into a 6-slot ring, 6 x 16 KB in flight;
+//               unswizzled);
 //   warp 1      allocates 512 TMEM columns; one thread issues
-//               tcgen05.mma M=128 N=256 K=16 from a 2-slot bf16 operand ring;
+//               tcgen05.mma M=128 N=256 K=16 and frees a token slot and a
+//               widened slot per k-block;
 //   warps 2..5  epilogue (scales, SwiGLU, stores through shared memory);
-//   warps 6..9  converters: for each k-block, load the 128x64 token tile by
-//               TMA into the bf16 operand slot and widen the E4M3 weight slot
-//               into the 128-byte-swizzled bf16 layout the MMA reads.
+//   warps 6..13 converters: widen each E4M3 slot into the 128-byte-swizzled
+//               bf16 layout the MMA reads (each thread loads its 8 chunks of
+//               8 codes before converting any, to keep the loads in flight);
+//   warp 14     TMA producer of the 128x64 token tiles.
 // E4M3 -> bf16: the byte's sign, exponent and mantissa are moved into bf16
 // positions (exponent bias 7 kept), then one bf16x2 multiply by 2^120 rebiases
 // to 127; subnormal codes come out exact because the multiply sees them as
@@ -37,27 +41,31 @@ using namespace tc;
 constexpr int QBM = 128;
 constexpr int QBK = 64;
 constexpr int QBN = 256;
-constexpr int QNF = 6;                               // E4M3 weight slots
-constexpr int QNB = 2;                               // bf16 operand slots
+constexpr int QNF = 5;                               // E4M3 weight slots
+constexpr int QNA = 3;                               // bf16 token-tile slots
+constexpr int QNB = 2;                               // widened bf16 weight slots
 constexpr uint32_t QA_STAGE = QBM * QBK * 2;         // 16 KB token tile (bf16)
 constexpr uint32_t QB_STAGE = QBN * QBK * 2;         // 32 KB weight tile (bf16, widened)
 constexpr uint32_t QF_STAGE = QBN * QBK;             // 16 KB weight tile (E4M3)
-constexpr int kQThreads = 320;
-constexpr int kConvThreads = 128;                    // warps 6..9
+constexpr int kQThreads = 480;
+constexpr int kConvWarp0 = 6;
+constexpr int kConvThreads = 256;                    // warps 6..13
+constexpr int kTokWarp = 14;
 constexpr uint32_t kQTmemCols = 512;
 constexpr int kQMaxGroups = kMaxExperts + 1;
 constexpr uint32_t kQCtrlBytes = 256 + 4 * (kQMaxGroups + 1 + 3 * kQMaxGroups);
 constexpr uint32_t kQStageWords = 32 * 33;
 constexpr uint32_t kQEpiBytes = 4 * kQStageWords * 4;
 constexpr uint32_t kQSmemBytes =
-    QNF * QF_STAGE + QNB * (QA_STAGE + QB_STAGE) + kQEpiBytes + kQCtrlBytes + 1024;
+    QNF * QF_STAGE + QNA * QA_STAGE + QNB * QB_STAGE + kQEpiBytes + kQCtrlBytes + 1024;
 static_assert(kQSmemBytes <= 227 * 1024, "shared memory budget");
-constexpr uint64_t kSettleNs = 20000;                // failure path: let copies land
 
 enum QMode { kQGateUp = 0, kQDown = 1 };
 
+constexpr int kQBoxes = 4;                           // token boxes of 128, 64, 32, 16 rows
+
 struct QParams {
-  CUtensorMap a_map[2];     // [0] routed grouped rows, [1] shared-expert rows (bf16)
+  CUtensorMap a_map[2][kQBoxes];   // [kind][box]: routed grouped rows / shared-expert rows (bf16)
   CUtensorMap b_map[2];     // E4M3 gate (gate/up) or down weights, box 64 B x 128 / 256 rows
   CUtensorMap u_map[2];     // E4M3 up weights (gate/up only)
   const float* b_scale[2];  // per-row scales of b_map's tensor
@@ -76,12 +84,6 @@ struct QParams {
 
 __device__ __forceinline__ int q_n_tiles(int mode, int N) {
   return mode == kQGateUp ? N / 128 : (N + QBN - 1) / QBN;
-}
-
-// Arms `bar` for `bytes` more transaction bytes without arriving.
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
 }
 
 // Generic-proxy shared-memory writes become visible to the async proxy
@@ -112,12 +114,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const v
   return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ void settle(uint64_t ns) {
-  const uint64_t t0 = globaltimer_ns();
-  while (globaltimer_ns() - t0 < ns) {
-  }
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(kQThreads, 1)
 grouped_gemm_fp8w_kernel(const __grid_constant__ QParams p) {
@@ -126,25 +122,28 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ QParams p) {
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t sB = base;                                   // QNB x 32 KB (1024-aligned)
-  const uint32_t sA = sB + QNB * QB_STAGE;                    // QNB x 16 KB
-  const uint32_t sF = sA + QNB * QA_STAGE;                    // QNF x 16 KB
+  const uint32_t sA = sB + QNB * QB_STAGE;                    // QNA x 16 KB
+  const uint32_t sF = sA + QNA * QA_STAGE;                    // QNF x 16 KB
   uint8_t* f8 = smem + (sF - base);
   uint8_t* bf = smem;
-  uint32_t* epi_stage =
-      reinterpret_cast<uint32_t*>(smem + QNB * (QA_STAGE + QB_STAGE) + QNF * QF_STAGE);
+  uint32_t* epi_stage = reinterpret_cast<uint32_t*>(smem + (sF - base) + QNF * QF_STAGE);
   uint8_t* ctrl = reinterpret_cast<uint8_t*>(epi_stage) + kQEpiBytes;
   const uint32_t bar0 = smem_u32(ctrl);
-  // barriers: wfull[QNF], wempty[QNF], full[QNB], empty[QNB], accf[2], acce[2], drain
+  // barriers: wfull[QNF], wempty[QNF], afull[QNA], aempty[QNA], full[QNB],
+  // empty[QNB], accf[2], acce[2], drain
+  constexpr int kNB = 2 * QNF + 2 * QNA + 2 * QNB;
   auto wfull_bar = [&](int s) { return bar0 + 8u * s; };
   auto wempty_bar = [&](int s) { return bar0 + 8u * (QNF + s); };
-  auto full_bar = [&](int s) { return bar0 + 8u * (2 * QNF + s); };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (2 * QNF + QNB + s); };
-  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * QNF + 2 * QNB + b); };
-  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * QNF + 2 * QNB + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * QNF + 2 * QNB + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * QNF + 2 * QNB + 5));
-  volatile int* abort_flag =
-      reinterpret_cast<volatile int*>(ctrl + 8 * (2 * QNF + 2 * QNB + 5) + 4);
+  auto afull_bar = [&](int s) { return bar0 + 8u * (2 * QNF + s); };
+  auto aempty_bar = [&](int s) { return bar0 + 8u * (2 * QNF + QNA + s); };
+  auto full_bar = [&](int s) { return bar0 + 8u * (2 * QNF + 2 * QNA + s); };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (2 * QNF + 2 * QNA + QNB + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (kNB + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (kNB + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (kNB + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (kNB + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 8 * (kNB + 5) + 4);
+  static_assert(8 * (kNB + 5) + 8 <= 256, "barriers fit the control header");
   int* s_tile_start = reinterpret_cast<int*>(ctrl + 256);
   int* s_row0 = s_tile_start + (kQMaxGroups + 1);
   int* s_rows = s_row0 + kQMaxGroups;
@@ -171,7 +170,11 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ QParams p) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < QNF; ++s) {
       mbar_init(wfull_bar(s), 1);
-      mbar_init(wempty_bar(s), kConvThreads / 32);
+      mbar_init(wempty_bar(s), kConvThreads / 32);   // one arrival per converter warp
+    }
+    for (int s = 0; s < QNA; ++s) {
+      mbar_init(afull_bar(s), 1);
+      mbar_init(aempty_bar(s), 1);
     }
     for (int s = 0; s < QNB; ++s) {
       mbar_init(full_bar(s), kConvThreads / 32);
@@ -189,7 +192,7 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ QParams p) {
     prefetch_tensormap(&p.b_map[0]);
     if (MODE == kQGateUp) prefetch_tensormap(&p.u_map[0]);
   }
-  if (warp == 6 && lane == 0) prefetch_tensormap(&p.a_map[0]);
+  if (warp == kTokWarp && lane == 0) prefetch_tensormap(&p.a_map[0][0]);
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kQTmemCols);
     tmem_relinquish();
@@ -278,18 +281,20 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ QParams p) {
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * QBN);
         for (int kb = 0; kb < nk; ++kb, ++i) {
-          const int bs = i % QNB;
-          if (!mbar_wait(full_bar(bs), (uint32_t)(i / QNB) & 1u, abort_flag, p.timeout_ns)) {
+          const int bs = i % QNB, as = i % QNA;
+          if (!mbar_wait(afull_bar(as), (uint32_t)(i / QNA) & 1u, abort_flag, p.timeout_ns) ||
+              !mbar_wait(full_bar(bs), (uint32_t)(i / QNB) & 1u, abort_flag, p.timeout_ns)) {
             failed = true;
             break;
           }
           tc_fence_after();
-          const uint64_t a_desc = sdesc_k128(sA + bs * QA_STAGE);
+          const uint64_t a_desc = sdesc_k128(sA + as * QA_STAGE);
           const uint64_t b_desc = sdesc_k128(sB + bs * QB_STAGE);
 #pragma unroll
           for (int kk = 0; kk < QBK / 16; ++kk)
             mma_bf16(d_tmem, a_desc + (uint64_t)(2 * kk), b_desc + (uint64_t)(2 * kk), idesc,
                      (kb | kk) != 0 ? 1u : 0u);
+          mma_commit(aempty_bar(as));
           mma_commit(empty_bar(bs));
         }
         if (failed) break;
@@ -302,43 +307,87 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ QParams p) {
         mbar_wait(drain_bar, 0, nullptr, p.timeout_ns);
       }
     }
-  } else if (warp >= 6) {
-    // ---------------- converters (warps 6..9) ----------------
-    const int ct = threadIdx.x - 6 * 32;
+  } else if (warp == kTokWarp) {
+    if (lane == 0) {
+      // ---------------- token-tile producer ----------------
+      int issued = 0;
+      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
+        int g, m, n;
+        decode(t, g, m, n);
+        const int kind = g < p.E ? 0 : 1;
+        const int nk = p.K[kind] / QBK;
+        const int a_row = s_row0[g] + m * QBM;
+        // only the tile's valid rows, rounded up to 16 (decode tiles hold a
+        // few rows); rows past them keep stale data and give discarded rows
+        const int n_load = (min(QBM, s_rows[g] - m * QBM) + 15) & ~15;
+        for (int kb = 0; kb < nk; ++kb, ++issued) {
+          const int as = issued % QNA;
+          if (!mbar_wait(aempty_bar(as), ((uint32_t)(issued / QNA) & 1u) ^ 1u, abort_flag,
+                         p.timeout_ns)) {
+            failed = true;
+            break;
+          }
+          mbar_arrive_expect_tx(afull_bar(as), (uint32_t)n_load * (QBK * 2));
+          int off = 0;
+#pragma unroll
+          for (int b = 0; b < kQBoxes; ++b) {
+            const int box = 128 >> b;
+            while (n_load - off >= box) {
+              tma_load_2d(sA + as * QA_STAGE + (uint32_t)off * (QBK * 2), &p.a_map[kind][b],
+                          afull_bar(as), kb * QBK, a_row + off);
+              off += box;
+            }
+          }
+        }
+      }
+      if (failed) {
+        *abort_flag = 1;
+        record_error(p.status, kDevTimeout);
+      }
+      for (int s = 0; s < QNA; ++s) {
+        if (issued > s) {
+          const int armed = (issued - 1 - s) / QNA + 1;
+          mbar_wait(afull_bar(s), (uint32_t)((armed - 1) & 1), nullptr, p.timeout_ns);
+        }
+      }
+    }
+  } else if (warp >= kConvWarp0) {
+    // ---------------- converters (warps 6..13) ----------------
+    const int ct = threadIdx.x - kConvWarp0 * 32;
     int i = 0;
     for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
       int g, m, n;
       decode(t, g, m, n);
       const int kind = g < p.E ? 0 : 1;
       const int nk = p.K[kind] / QBK;
-      const int a_row = s_row0[g] + m * QBM;
       for (int kb = 0; kb < nk; ++kb, ++i) {
         const int fs = i % QNF, bs = i % QNB;
         if (!warp_wait(empty_bar(bs), ((uint32_t)(i / QNB) & 1u) ^ 1u, abort_flag,
-                       p.timeout_ns)) {
+                       p.timeout_ns) ||
+            !warp_wait(wfull_bar(fs), (uint32_t)(i / QNF) & 1u, abort_flag, p.timeout_ns)) {
           failed = true;
           break;
         }
-        if (ct == 0) {
-          mbar_expect_tx(full_bar(bs), QA_STAGE);
-          tma_load_2d(sA + bs * QA_STAGE, &p.a_map[kind], full_bar(bs), kb * QBK, a_row);
-        }
-        if (!warp_wait(wfull_bar(fs), (uint32_t)(i / QNF) & 1u, abort_flag, p.timeout_ns)) {
-          failed = true;
-          break;
-        }
-        // 256 rows x 8 chunks of 8 codes -> 8 bf16 (16 bytes) at the swizzled chunk
+        // 256 rows x 8 chunks of 8 codes -> 8 bf16 (16 bytes) at the swizzled
+        // chunk; each thread loads its 8 chunks before converting any
+        constexpr int kPer = QBN * 8 / kConvThreads;
         const uint8_t* src = f8 + fs * QF_STAGE;
         uint8_t* dst = bf + bs * QB_STAGE;
-#pragma unroll 4
-        for (int q = ct; q < QBN * 8; q += kConvThreads) {
+        uint2 v[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+          const int q = ct + kConvThreads * j;
+          v[j] = *reinterpret_cast<const uint2*>(src + (q >> 3) * 64 + (q & 7) * 8);
+        }
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+          const int q = ct + kConvThreads * j;
           const int r = q >> 3, c = q & 7;
-          const uint2 v = *reinterpret_cast<const uint2*>(src + r * 64 + c * 8);
           uint4 o;
-          o.x = e4m3x2_hi_to_bf16x2(prmt(v.x, 0x1404u));
-          o.y = e4m3x2_hi_to_bf16x2(prmt(v.x, 0x3424u));
-          o.z = e4m3x2_hi_to_bf16x2(prmt(v.y, 0x1404u));
-          o.w = e4m3x2_hi_to_bf16x2(prmt(v.y, 0x3424u));
+          o.x = e4m3x2_hi_to_bf16x2(prmt(v[j].x, 0x1404u));
+          o.y = e4m3x2_hi_to_bf16x2(prmt(v[j].x, 0x3424u));
+          o.z = e4m3x2_hi_to_bf16x2(prmt(v[j].y, 0x1404u));
+          o.w = e4m3x2_hi_to_bf16x2(prmt(v[j].y, 0x3424u));
           *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = o;
         }
         fence_proxy_async_smem();
@@ -352,7 +401,6 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ QParams p) {
     if (failed) {
       *abort_flag = 1;
       if (lane == 0) record_error(p.status, kDevTimeout);
-      settle(kSettleNs);   // the token-tile copies this warp issued land before teardown
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
@@ -381,22 +429,25 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ QParams p) {
         const size_t ld2 = (size_t)p.ld_out[kind] / 2;
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
-          uint32_t gv[32], uv[32];
-          tmem_ld_32x32b_x32(tbase + (uint32_t)c, gv);
-          tmem_ld_32x32b_x32(tbase + 128u + (uint32_t)c, uv);
-          tmem_ld_wait();
+#pragma unroll 1
+          for (int hh = 0; hh < 32; hh += 16) {   // 16 columns at a time (registers)
+            uint32_t gv[16], uv[16];
+            tmem_ld_32x32b_x16(tbase + (uint32_t)(c + hh), gv);
+            tmem_ld_32x32b_x16(tbase + 128u + (uint32_t)(c + hh), uv);
+            tmem_ld_wait();
 #pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) {
-            const float4 a = __ldg(reinterpret_cast<const float4*>(sg + c) + j4);
-            const float4 b = __ldg(reinterpret_cast<const float4*>(su + c) + j4);
-            const float h0 = silu_f(bits_f(gv[4 * j4]) * a.x) * (bits_f(uv[4 * j4]) * b.x);
-            const float h1 = silu_f(bits_f(gv[4 * j4 + 1]) * a.y) * (bits_f(uv[4 * j4 + 1]) * b.y);
-            const float h2 = silu_f(bits_f(gv[4 * j4 + 2]) * a.z) * (bits_f(uv[4 * j4 + 2]) * b.z);
-            const float h3 = silu_f(bits_f(gv[4 * j4 + 3]) * a.w) * (bits_f(uv[4 * j4 + 3]) * b.w);
-            __nv_bfloat162 p0 = __floats2bfloat162_rn(h0, h1);
-            __nv_bfloat162 p1 = __floats2bfloat162_rn(h2, h3);
-            st[lane * 33 + 2 * j4] = *reinterpret_cast<uint32_t*>(&p0);
-            st[lane * 33 + 2 * j4 + 1] = *reinterpret_cast<uint32_t*>(&p1);
+            for (int j4 = 0; j4 < 4; ++j4) {
+              const float4 a = __ldg(reinterpret_cast<const float4*>(sg + c + hh) + j4);
+              const float4 b = __ldg(reinterpret_cast<const float4*>(su + c + hh) + j4);
+              const float h0 = silu_f(bits_f(gv[4 * j4]) * a.x) * (bits_f(uv[4 * j4]) * b.x);
+              const float h1 = silu_f(bits_f(gv[4 * j4 + 1]) * a.y) * (bits_f(uv[4 * j4 + 1]) * b.y);
+              const float h2 = silu_f(bits_f(gv[4 * j4 + 2]) * a.z) * (bits_f(uv[4 * j4 + 2]) * b.z);
+              const float h3 = silu_f(bits_f(gv[4 * j4 + 3]) * a.w) * (bits_f(uv[4 * j4 + 3]) * b.w);
+              __nv_bfloat162 p0 = __floats2bfloat162_rn(h0, h1);
+              __nv_bfloat162 p1 = __floats2bfloat162_rn(h2, h3);
+              st[lane * 33 + hh / 2 + 2 * j4] = *reinterpret_cast<uint32_t*>(&p0);
+              st[lane * 33 + hh / 2 + 2 * j4 + 1] = *reinterpret_cast<uint32_t*>(&p1);
+            }
           }
           __syncwarp();
           const size_t col2 = ((size_t)n * 128 + (size_t)c) / 2 + (size_t)(lane & 15);
@@ -415,16 +466,19 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ QParams p) {
 #pragma unroll 1
         for (int c = 0; c < QBN; c += 32) {
           if (c >= ncols) break;
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tbase + (uint32_t)c, v);
-          tmem_ld_wait();
+#pragma unroll 1
+          for (int hh = 0; hh < 32; hh += 16) {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(tbase + (uint32_t)(c + hh), v);
+            tmem_ld_wait();
 #pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) {
-            const float4 a = __ldg(reinterpret_cast<const float4*>(sd + c) + j4);
-            st[lane * 33 + 4 * j4] = __float_as_uint(bits_f(v[4 * j4]) * a.x);
-            st[lane * 33 + 4 * j4 + 1] = __float_as_uint(bits_f(v[4 * j4 + 1]) * a.y);
-            st[lane * 33 + 4 * j4 + 2] = __float_as_uint(bits_f(v[4 * j4 + 2]) * a.z);
-            st[lane * 33 + 4 * j4 + 3] = __float_as_uint(bits_f(v[4 * j4 + 3]) * a.w);
+            for (int j4 = 0; j4 < 4; ++j4) {
+              const float4 a = __ldg(reinterpret_cast<const float4*>(sd + c + hh) + j4);
+              st[lane * 33 + hh + 4 * j4] = __float_as_uint(bits_f(v[4 * j4]) * a.x);
+              st[lane * 33 + hh + 4 * j4 + 1] = __float_as_uint(bits_f(v[4 * j4 + 1]) * a.y);
+              st[lane * 33 + hh + 4 * j4 + 2] = __float_as_uint(bits_f(v[4 * j4 + 2]) * a.z);
+              st[lane * 33 + hh + 4 * j4 + 3] = __float_as_uint(bits_f(v[4 * j4 + 3]) * a.w);
+            }
           }
           __syncwarp();
           const size_t col = (size_t)n * QBN + (size_t)c + (size_t)lane;
@@ -467,6 +521,12 @@ cudaError_t launch_q(const QParams& p, cudaStream_t s) {
 
 // Row-major E4M3 matrix [rows, inner] read in unswizzled boxes of 64 bytes x
 // box_rows; rows past the end read as zero.
+bool token_maps_q(CUtensorMap (&m)[kQBoxes], const void* ptr, uint64_t inner, uint64_t rows) {
+  bool ok = true;
+  for (int b = 0; b < kQBoxes; ++b) ok &= make_map(&m[b], ptr, inner, rows, 128u >> b);
+  return ok;
+}
+
 bool make_map_e4m3(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows,
                    uint32_t box_rows) {
   auto fn = encode_fn();
@@ -499,8 +559,8 @@ cudaError_t launch_gemm_fp8w(const moe_config_t& c, const ExpertArgs& a, int whi
   p.status = a.status;
   p.timeout_ns = kWaitTimeoutNs;
   if (which == kGemmGateUp) {
-    ok &= make_map(&p.a_map[0], a.x_perm, d, A, QBM);
-    ok &= make_map(&p.a_map[1], a.x, d, T, QBM);
+    ok &= token_maps_q(p.a_map[0], a.x_perm, d, A);
+    ok &= token_maps_q(p.a_map[1], a.x, d, T);
     ok &= make_map_e4m3(&p.b_map[0], a.w_gate, d, (uint64_t)E * F, 128);
     ok &= make_map_e4m3(&p.u_map[0], a.w_up, d, (uint64_t)E * F, 128);
     p.b_scale[0] = sc.gate_scale;
@@ -526,15 +586,15 @@ cudaError_t launch_gemm_fp8w(const moe_config_t& c, const ExpertArgs& a, int whi
     p.N[1] = has_shared ? Fs : 128;
     p.b_rows_per_expert = F;
   } else {
-    ok &= make_map(&p.a_map[0], a.h, F, A, QBM);
+    ok &= token_maps_q(p.a_map[0], a.h, F, A);
     ok &= make_map_e4m3(&p.b_map[0], a.w_down, F, (uint64_t)E * d, QBN);
     p.b_scale[0] = sc.down_scale;
     if (has_shared) {
-      ok &= make_map(&p.a_map[1], a.h_shared, Fs, T, QBM);
+      ok &= token_maps_q(p.a_map[1], a.h_shared, Fs, T);
       ok &= make_map_e4m3(&p.b_map[1], a.ws_down, Fs, d, QBN);
       p.b_scale[1] = sc.shared_down_scale;
     } else {
-      p.a_map[1] = p.a_map[0];
+      for (int b = 0; b < kQBoxes; ++b) p.a_map[1][b] = p.a_map[0][b];
       p.b_map[1] = p.b_map[0];
       p.b_scale[1] = p.b_scale[0];
     }
