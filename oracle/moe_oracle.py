@@ -191,6 +191,64 @@ def update_score_bias(score_bias: np.ndarray, load: np.ndarray, gamma: float) ->
     return np.asarray(score_bias, dtype=np.float64) - gamma * np.sign(load - np.mean(load))
 
 
+# ---------------------------------------------------------------------------
+# Expert-choice routing ([routing]: "让每个专家挑走它最想要的固定数量 token" -
+# each expert takes the fixed number of tokens it wants most, which balances
+# the load by construction; a token may be taken by no expert).
+# ---------------------------------------------------------------------------
+
+def expert_choice_capacity(T: int, E: int, k: int, capacity: Optional[int] = None) -> int:
+    """Tokens each expert takes: the given capacity, else ceil(T * k / E)
+    (as many slots as token-choice top-k would fill on average); at most T."""
+    c = int(math.ceil(T * k / E)) if capacity is None else int(capacity)
+    return max(0, min(c, T))
+
+
+def expert_choice(scores: np.ndarray, C: int) -> Dict[str, np.ndarray]:
+    """Expert e takes the C tokens with the largest scores[t, e], ties to the
+    lower token index; its tokens are listed in ascending token order.
+
+      tokens[e, i]  the i-th token of expert e
+      weights[e, i] scores[tokens[e, i], e], the combine weight
+      picked[t]     how many experts took token t
+    """
+    scores = np.asarray(scores, dtype=np.float64)
+    T, E = scores.shape
+    tokens = np.empty((E, C), dtype=np.int64)
+    for e in range(E):
+        best = sorted(range(T), key=lambda t: (-scores[t, e], t))[:C]
+        tokens[e] = sorted(best)
+    weights = np.take_along_axis(scores.T, tokens, axis=1)
+    picked = np.bincount(tokens.ravel(), minlength=T) if C > 0 else np.zeros(T, np.int64)
+    return {"tokens": tokens, "weights": weights, "picked": picked}
+
+
+def moe_layer_expert_choice(x: np.ndarray, w_router: np.ndarray, experts, C: int, gate: str,
+                            shared=None, tokens: Optional[Sequence[int]] = None,
+                            logits: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """y_t = sum over the experts e that took t of scores[t, e] * E_e(x_t)
+    (+ the shared expert), computed per expert over its chosen tokens."""
+    x = np.asarray(x, dtype=np.float64)
+    T = x.shape[0]
+    z = router_logits(x, w_router) if logits is None else np.asarray(logits, np.float64)
+    scores = gate_scores(z, gate)
+    ec = expert_choice(scores, C)
+    toks = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    pos = {int(t): i for i, t in enumerate(toks)}
+    y = np.zeros((len(toks), x.shape[1]), dtype=np.float64)
+    for e in range(z.shape[1]):
+        rows = [int(t) for t in ec["tokens"][e] if int(t) in pos]
+        if not rows:
+            continue
+        out = swiglu_ffn(x[rows], *experts[e])
+        for i, t in enumerate(rows):
+            y[pos[t]] += scores[t, e] * out[i]
+    if shared is not None:
+        y += swiglu_ffn(x[toks], *shared)
+    ec.update(y=y, scores=scores, logits=z, mean_prob=mean_router_prob(scores))
+    return ec
+
+
 def mean_router_prob(scores: np.ndarray) -> np.ndarray:
     """P_e = (1/T) sum_t score[t,e], the batch-mean router probability that
     the load statistics use ([moe10] "辅助损失", definition of P_i)."""

@@ -545,3 +545,58 @@ def test_dequantize_rows_scales_each_output_channel():
     codes = np.array([[0x38, 0x40], [0x30, 0xB8]], dtype=np.uint8)
     np.testing.assert_array_equal(O.dequantize_rows(codes, [3.0, 0.25]),
                                   [[3.0, 6.0], [0.125, -0.25]])
+
+
+# ---------------------------------------------------------------------------
+# Expert-choice routing ([routing]: each expert takes the fixed number of
+# tokens it wants most)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,E,C", [(6, 3, 2), (7, 2, 3), (5, 4, 5), (8, 3, 0)])
+def test_expert_choice_brute_force(T, E, C):
+    rng = np.random.default_rng(T * 10 + E)
+    s = rng.uniform(size=(T, E))
+    ec = O.expert_choice(s, C)
+    for e in range(E):
+        best = max(itertools.combinations(range(T), C), key=lambda c: sum(s[t, e] for t in c))
+        assert list(ec["tokens"][e]) == sorted(best)
+        np.testing.assert_array_equal(ec["weights"][e], s[ec["tokens"][e], e])
+    assert ec["picked"].sum() == E * C            # balanced: every expert exactly C
+
+
+def test_expert_choice_ties_go_to_lower_token():
+    s = np.array([[0.5, 0.1], [0.5, 0.9], [0.5, 0.9], [0.2, 0.9]])
+    ec = O.expert_choice(s, 2)
+    assert list(ec["tokens"][0]) == [0, 1]
+    assert list(ec["tokens"][1]) == [1, 2]
+    assert list(ec["picked"]) == [1, 2, 1, 0]      # token 3 taken by no expert
+
+
+def test_expert_choice_capacity_default():
+    assert O.expert_choice_capacity(16384, 64, 1) == 256
+    assert O.expert_choice_capacity(10, 4, 2) == 5     # ceil(20 / 4)
+    assert O.expert_choice_capacity(10, 3, 2) == 7     # ceil(20 / 3)
+    assert O.expert_choice_capacity(4, 2, 2, 9) == 4   # at most T
+
+
+def test_expert_choice_full_capacity_is_full_softmax_mixture():
+    # C = T: every expert takes every token, so y = sum_e p_e E_e(x), which is
+    # token-choice top-E with renormalisation (the weights already sum to 1)
+    x, wr, ex, _ = _tiny_layer(20, T=9, E=4)
+    T = x.shape[0]
+    a = O.moe_layer_expert_choice(x, wr, ex, C=T, gate="softmax")["y"]
+    b = O.moe_layer_forward(x, wr, ex, k=4, gate="softmax", renormalize=True)["y"]
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+def test_expert_choice_layer_matches_token_loop():
+    x, wr, ex, sh = _tiny_layer(21, T=12, E=4)
+    r = O.moe_layer_expert_choice(x, wr, ex, C=5, gate="sigmoid", shared=sh)
+    s = O.sigmoid(O.router_logits(x, wr))
+    want = np.zeros_like(r["y"])
+    for t in range(x.shape[0]):
+        for e in range(4):
+            if t in set(r["tokens"][e].tolist()):
+                want[t] += s[t, e] * O.swiglu_ffn(x[t:t + 1], *ex[e])[0]
+        want[t] += O.swiglu_ffn(x[t:t + 1], *sh)[0]
+    np.testing.assert_allclose(r["y"], want, rtol=1e-12, atol=1e-12)
