@@ -43,6 +43,9 @@ WORKLOAD_TEXT = {
     "dsv3_prefill_noaux": "DeepSeek-V3-shaped MoE prefill layer with DeepSeek-V3's router "
                           "(T=8192, d=7168, E=256 top-8 ranked by sigmoid + selection bias, "
                           "8 groups / 4 kept, d_ff=2048, 1 shared expert, renorm x2.5, bf16)",
+    "switch_expert_choice": "Switch-shaped layer routed by expert choice (T=16384, d=2048, "
+                            "E=64, each expert takes C=T/E=256 tokens, d_ff=8192, softmax "
+                            "scores, bf16)",
     "dsv3_decode_fp8": "DeepSeek-V3-shaped decode layer with E4M3 expert weights (T=64, "
                        "d=7168, E=256 top-8, d_ff=2048, 1 shared expert, sigmoid, renorm x2.5, "
                        "bf16 activations, one fp32 scale per weight row)",
@@ -259,11 +262,17 @@ def time_oracle(shape, inputs, sample_tokens: int, steps: int, warmup: int = 0):
     for i in range(warmup + steps):
         toks = np.sort(rng.choice(shape.T, size=min(sample_tokens, shape.T), replace=False))
         t0 = time.perf_counter()
-        O.moe_layer_forward(x, wr, experts, k=shape.k, gate=shape.gate,
-                            renormalize=shape.renormalize, routed_scaling_factor=shape.rsf,
-                            capacity=cap, router_bias=bias, shared=shared, tokens=toks,
-                            score_bias=to_f64(inputs.get("score_bias")),
-                            n_group=max(shape.n_group, 1), topk_group=shape.topk_group)
+        if getattr(shape, "routing", "token") == "expert":
+            O.moe_layer_expert_choice(x, wr, experts,
+                                      O.expert_choice_capacity(shape.T, shape.E, shape.k),
+                                      shape.gate, shared=shared, tokens=toks)
+        else:
+            O.moe_layer_forward(x, wr, experts, k=shape.k, gate=shape.gate,
+                                renormalize=shape.renormalize, routed_scaling_factor=shape.rsf,
+                                capacity=cap, router_bias=bias, shared=shared, tokens=toks,
+                                score_bias=to_f64(inputs.get("score_bias")),
+                                n_group=max(shape.n_group, 1), topk_group=shape.topk_group,
+                                shared_gate=to_f64(inputs.get("shared_gate")))
         if i >= warmup:
             times.append(time.perf_counter() - t0)
     return times
@@ -357,8 +366,9 @@ def main(argv=None):
     counts = torch.empty(E, dtype=torch.int32, device=dev)
     drops = torch.empty(E, dtype=torch.int32, device=dev)
     mean_prob = torch.empty(E, dtype=torch.float32, device=dev)
-    topk_idx = torch.empty((T, k), dtype=torch.int32, device=dev)
-    topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    token_choice = getattr(shape, "routing", "token") == "token"   # expert choice: no top-k
+    topk_idx = torch.empty((T, k), dtype=torch.int32, device=dev) if token_choice else None
+    topk_w = torch.empty((T, k), dtype=torch.float32, device=dev) if token_choice else None
     stream = torch.cuda.current_stream(dev)
     NS = B.MOE_NUM_STAGES
 

@@ -81,6 +81,14 @@ typedef enum { MOE_BF16 = 0, MOE_FP32 = 1 } moe_dtype_t;
  * MOE_BF16; the products are exact in bf16 and the scale is applied to the
  * fp32 accumulator of each output. */
 typedef enum { MOE_WEIGHTS_ACT = 0, MOE_WEIGHTS_FP8_E4M3 = 1 } moe_weight_format_t;
+/* Who chooses.  MOE_ROUTE_TOKEN_CHOICE: each token takes its top_k experts
+ * (selection rule below).  MOE_ROUTE_EXPERT_CHOICE ("MoE 路由为什么是最难的
+ * 部分", the routing article: each expert takes the fixed number of tokens it
+ * wants most, which balances the load by construction; a token may be taken
+ * by no expert): expert e takes the C = moe_expert_choice_capacity(cfg)
+ * tokens with the largest fp32 score s[t, e] (ties to the lower token), and
+ * y_t = sum over the experts that took t of s[t, e] * E_e(x_t) (+ shared). */
+typedef enum { MOE_ROUTE_TOKEN_CHOICE = 0, MOE_ROUTE_EXPERT_CHOICE = 1 } moe_routing_t;
 
 /* Layer description.  All fields are plain 32-bit values. */
 typedef struct {
@@ -101,6 +109,8 @@ typedef struct {
   int32_t topk_group;     /* groups kept per token when n_group > 1 (1..n_group;
                              top_k <= topk_group * n_experts / n_group)           */
   int32_t weight_format;  /* moe_weight_format_t of the expert weights          */
+  int32_t routing;        /* moe_routing_t; expert choice requires T <= 32768, no
+                             score bias or groups, and no topk_idx / topk_w outputs */
 } moe_config_t;
 
 /* Per-output-channel scales of E4M3 expert weights (weight_format ==
@@ -125,6 +135,11 @@ MOE_API const char* moe_status_string(moe_status_t st);
  * that order ("负载不均：路由坍缩与丢 token": 2 x 1.25 = 2.5 is rounded up to 3).
  * Returns -1 for T < 0, E <= 0 or capacity_factor < 0 (or NaN). */
 MOE_API int32_t moe_capacity(int32_t T, int32_t E, double capacity_factor);
+
+/* Tokens each expert takes under expert-choice routing: cfg->capacity when
+ * >= 0, else ceil(T * top_k / E) (as many slots as token choice fills on
+ * average), at most T.  -1 for an invalid configuration. */
+MOE_API int32_t moe_expert_choice_capacity(const moe_config_t* cfg);
 
 /* Bytes of workspace every call below needs for this configuration. */
 MOE_API moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
@@ -175,6 +190,17 @@ MOE_API moe_status_t moe_topk_from_logits(const moe_config_t* cfg, const float* 
                                   const float* score_bias,
                                   int32_t* topk_idx, float* topk_w, float* mean_prob,
                                   void* ws, size_t ws_bytes, void* stream);
+
+/* Expert-choice selection from fp32 logits [T, E] (cfg->routing must be
+ * MOE_ROUTE_EXPERT_CHOICE; C = moe_expert_choice_capacity(cfg)):
+ *   tokens [E, C] int32: expert e's tokens in ascending order;
+ *   weights [E, C] fp32: s[tokens[e, i], e], the combine weights;
+ *   mean_prob [E] fp32 or NULL: (1/T) sum_t s[t, e].
+ * The selection compares fp32 scores (softmax or sigmoid of the logits). */
+MOE_API moe_status_t moe_expert_choice_from_logits(const moe_config_t* cfg, const float* logits,
+                                                   int32_t* tokens, float* weights,
+                                                   float* mean_prob, void* ws, size_t ws_bytes,
+                                                   void* stream);
 
 /* One step of the auxiliary-loss-free bias ("DeepSeek-V3 的无辅助损失偏置":
  * after each batch an overloaded expert's bias is lowered by gamma and an
@@ -295,7 +321,8 @@ MOE_API moe_status_t moe_balance_loss(const moe_config_t* cfg, const int32_t* co
  *   scales: E4M3 weight scales (cfg->weight_format MOE_WEIGHTS_FP8_E4M3),
  *     else NULL;
  *   topk_idx [T, k], topk_w [T, k], counts [E], drops [E], mean_prob [E]
- *     are optional outputs (NULL = not returned). */
+ *     are optional outputs (NULL = not returned); under expert choice
+ *     topk_idx / topk_w must be NULL, counts[e] = C and drops[e] = 0. */
 MOE_API moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const void* w_router,
                                const float* router_bias, const float* score_bias,
                                const void* w_gate, const void* w_up, const void* w_down,

@@ -200,6 +200,34 @@ def test_group_fields_validated(E, k, n_group, topk_group, want):
     assert _ws_size(c)[0] == want
 
 
+def test_expert_choice_config_and_capacity():
+    lib = B.load_library()
+    c = _cfg(T=10, E=4, k=2, routing="expert")
+    assert lib.moe_expert_choice_capacity(ctypes.byref(c)) == 5        # ceil(10 * 2 / 4)
+    c.capacity = 3
+    assert lib.moe_expert_choice_capacity(ctypes.byref(c)) == 3
+    c.capacity = 99
+    assert lib.moe_expert_choice_capacity(ctypes.byref(c)) == 10       # at most T
+    big = _cfg(T=40000, E=4, k=2, routing="expert")
+    assert _ws_size(big)[0] == B.MOE_ERR_UNSUPPORTED
+    grouped = _cfg(E=8, k=2, routing="expert")
+    grouped.n_group, grouped.topk_group = 4, 2
+    assert _ws_size(grouped)[0] == B.MOE_ERR_INVALID_ARG
+    bad = _cfg()
+    bad.routing = 5
+    assert _ws_size(bad)[0] == B.MOE_ERR_INVALID_ARG
+    # token-choice entry points refuse an expert-choice configuration
+    ec = _cfg(routing="expert")
+    _, need = _ws_size(ec)
+    fake = 0x10000
+    assert lib.moe_topk_from_logits(ctypes.byref(ec), fake, None, fake, fake, None, fake, need,
+                                    None) == B.MOE_ERR_INVALID_ARG
+    # expert-choice layer forward rejects per-token top-k outputs
+    assert lib.moe_layer_forward(ctypes.byref(ec), fake, fake, None, None, fake, fake, fake,
+                                 None, None, None, None, None, fake, fake, None, None, None, None,
+                                 fake, need, None) == B.MOE_ERR_INVALID_ARG
+
+
 def test_config_from_shape_capacity():
     from workloads import SHAPES
     c = moe.config_from_shape(SHAPES["switch"])

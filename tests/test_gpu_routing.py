@@ -24,7 +24,8 @@ DEV = "cuda"
 
 # the layers routed by logit top-k (the DeepSeek-V3 score-bias router is
 # covered in test_gpu_noaux.py)
-LOGIT_SHAPES = [n for n, s in SHAPES.items() if s.n_group == 0 and s.score_bias_std is None]
+LOGIT_SHAPES = [n for n, s in SHAPES.items()
+                if s.n_group == 0 and s.score_bias_std is None and s.routing == "token"]
 
 
 def _logits(T, E, seed, quantize=None):

@@ -30,6 +30,8 @@ MOE_BF16 = 0
 MOE_FP32 = 1
 MOE_WEIGHTS_ACT = 0
 MOE_WEIGHTS_FP8_E4M3 = 1
+MOE_ROUTE_TOKEN_CHOICE = 0
+MOE_ROUTE_EXPERT_CHOICE = 1
 
 
 class MoEConfig(ctypes.Structure):
@@ -50,6 +52,7 @@ class MoEConfig(ctypes.Structure):
         ("n_group", c_int32),
         ("topk_group", c_int32),
         ("weight_format", c_int32),
+        ("routing", c_int32),
     ]
 
     def __repr__(self):
@@ -84,6 +87,9 @@ SIGNATURES = {
     "moe_topk_from_logits": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                        c_void_p, c_size_t, c_void_p]),
     "moe_update_score_bias": (c_int32, [CFG, c_void_p, c_void_p, c_float, c_void_p, c_void_p]),
+    "moe_expert_choice_capacity": (c_int32, [CFG]),
+    "moe_expert_choice_from_logits": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p,
+                                                c_void_p, c_size_t, c_void_p]),
     "moe_dispatch": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_dispatch_no_workspace": (c_int32, [CFG, c_void_p, c_void_p, c_void_p, c_void_p,

@@ -23,18 +23,20 @@ _TORCH_DT = {B.MOE_BF16: torch.bfloat16, B.MOE_FP32: torch.float32}
 
 
 _WF = {"act": B.MOE_WEIGHTS_ACT, "fp8": B.MOE_WEIGHTS_FP8_E4M3}
+_RT = {"token": B.MOE_ROUTE_TOKEN_CHOICE, "expert": B.MOE_ROUTE_EXPERT_CHOICE}
 
 
 def make_config(T: int, d: int, E: int, k: int, F: int, F_s: int = 0, gate: str = "softmax",
                 renormalize: bool = True, rsf: float = 1.0, capacity: int = -1,
                 act_dtype: str = "bf16", out_dtype: str = "fp32", n_group: int = 0,
-                topk_group: int = 0, weight_format: str = "act") -> MoEConfig:
+                topk_group: int = 0, weight_format: str = "act",
+                routing: str = "token") -> MoEConfig:
     return MoEConfig(T=T, d_model=d, n_experts=E, top_k=k, d_ff=F, d_ff_shared=F_s,
                      gate=B.MOE_GATE_SOFTMAX if gate == "softmax" else B.MOE_GATE_SIGMOID,
                      renormalize=1 if renormalize else 0, routed_scaling_factor=float(rsf),
                      capacity=int(capacity), act_dtype=_DT[act_dtype], out_dtype=_DT[out_dtype],
                      n_group=int(n_group), topk_group=int(topk_group),
-                     weight_format=_WF[weight_format])
+                     weight_format=_WF[weight_format], routing=_RT[routing])
 
 
 def config_from_shape(shape, out_dtype: str = "fp32", T: Optional[int] = None) -> MoEConfig:
@@ -46,7 +48,7 @@ def config_from_shape(shape, out_dtype: str = "fp32", T: Optional[int] = None) -
     return make_config(T, shape.d, shape.E, shape.k, shape.F, shape.F_s, shape.gate,
                        shape.renormalize, shape.rsf, cap, shape.dtype, out_dtype,
                        getattr(shape, "n_group", 0), getattr(shape, "topk_group", 0),
-                       getattr(shape, "weight_format", "act"))
+                       getattr(shape, "weight_format", "act"), getattr(shape, "routing", "token"))
 
 
 def act_dtype(cfg: MoEConfig) -> torch.dtype:
@@ -120,6 +122,29 @@ def moe_topk_from_logits(cfg, logits, score_bias, topk_idx, topk_w, mean_prob, w
         ctypes.byref(cfg), _ptr(logits, "logits"), _ptr(score_bias), _ptr(topk_idx),
         _ptr(topk_w), _ptr(mean_prob), ws.ptr, ws.nbytes, _stream(stream)),
         "moe_topk_from_logits")
+
+
+def moe_expert_choice_capacity(cfg) -> int:
+    return load_library().moe_expert_choice_capacity(ctypes.byref(cfg))
+
+
+def moe_expert_choice_from_logits(cfg, logits, tokens, weights, mean_prob, ws: Workspace,
+                                  stream=None) -> None:
+    check(load_library().moe_expert_choice_from_logits(
+        ctypes.byref(cfg), _ptr(logits, "logits"), _ptr(tokens), _ptr(weights), _ptr(mean_prob),
+        ws.ptr, ws.nbytes, _stream(stream)), "moe_expert_choice_from_logits")
+
+
+def expert_choice_from_logits(cfg, logits, ws: Optional[Workspace] = None):
+    dev = logits.device
+    ws = ws or Workspace(cfg, dev)
+    C, E = moe_expert_choice_capacity(cfg), cfg.n_experts
+    out = {"tokens": torch.empty((E, C), dtype=torch.int32, device=dev),
+           "weights": torch.empty((E, C), dtype=torch.float32, device=dev),
+           "mean_prob": _f32(E, dev)}
+    moe_expert_choice_from_logits(cfg, logits, out["tokens"] if C else None,
+                                  out["weights"] if C else None, out["mean_prob"], ws)
+    return out
 
 
 def moe_update_score_bias(cfg, counts, drops, gamma: float, score_bias, stream=None) -> None:
@@ -309,8 +334,9 @@ def layer_forward(cfg, x, w: LayerWeights, ws: Optional[Workspace] = None,
     T, E, k, d = cfg.T, cfg.n_experts, cfg.top_k, cfg.d_model
     out = {"y": y if y is not None else torch.empty((T, d), dtype=out_dtype(cfg), device=dev)}
     if stats:
-        out.update(topk_idx=_i32((T, k), dev), topk_w=_f32((T, k), dev), counts=_i32(E, dev),
-                   drops=_i32(E, dev), mean_prob=_f32(E, dev))
+        out.update(counts=_i32(E, dev), drops=_i32(E, dev), mean_prob=_f32(E, dev))
+        if cfg.routing == B.MOE_ROUTE_TOKEN_CHOICE:   # expert choice has no per-token top-k
+            out.update(topk_idx=_i32((T, k), dev), topk_w=_f32((T, k), dev))
     g = out.get
     moe_layer_forward(cfg, x, w.w_router, w.router_bias, w.score_bias, w.w_gate, w.w_up,
                       w.w_down, w.ws_gate, w.ws_up, w.ws_down, w.shared_gate, w.scales, out["y"],

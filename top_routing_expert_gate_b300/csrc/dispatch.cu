@@ -143,17 +143,17 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, int A, int E, int capac
   (void)status;
 }
 
-// One warp per grouped row, 16-byte vectors.
+// One warp per grouped row, 16-byte vectors; row r holds token perm[r] / k.
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
-                   const int32_t* __restrict__ offsets, int E, int k, int T, int row_vec,
-                   uint4* __restrict__ x_perm, int32_t* status) {
+                   const int32_t* __restrict__ offsets, int E, int k, int T, int rows_cap,
+                   int row_vec, uint4* __restrict__ x_perm, int32_t* status) {
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
   int n = offsets[E];
-  if (n < 0 || n > T * k) {
+  if (n < 0 || n > rows_cap) {
     if (blockIdx.x == 0 && threadIdx.x == 0) record_error(status, kDevBadIndex);
-    n = n < 0 ? 0 : T * k;
+    n = n < 0 ? 0 : rows_cap;
   }
   for (int r = blockIdx.x * warps + (threadIdx.x >> 5); r < n; r += gridDim.x * warps) {
     const int a = perm[r];
@@ -295,15 +295,16 @@ cudaError_t launch_dispatch(const moe_config_t& c, const int32_t* idx, int32_t* 
 
 cudaError_t launch_gather(const moe_config_t& c, const void* x, const int32_t* perm,
                           const int32_t* offsets, void* x_perm, int32_t* status,
-                          cudaStream_t s, LaunchCounter* lc) {
-  const int A = c.T * c.top_k;
-  if (A == 0) return cudaSuccess;
+                          cudaStream_t s, LaunchCounter* lc, int div) {
+  const int A = (int)grouped_rows(c);
+  if (A == 0 || c.T == 0) return cudaSuccess;
+  if (div <= 0) div = c.routing == MOE_ROUTE_EXPERT_CHOICE ? 1 : c.top_k;
   const int row_vec = (int)(c.d_model * act_bytes(c) / 16);
   int blocks = (A + 7) / 8;
   const int cap = sm_count() * 8;
   if (blocks > cap) blocks = cap;
-  gather_rows_kernel<<<blocks, 256, 0, s>>>((const uint4*)x, perm, offsets, c.n_experts,
-                                            c.top_k, c.T, row_vec, (uint4*)x_perm, status);
+  gather_rows_kernel<<<blocks, 256, 0, s>>>((const uint4*)x, perm, offsets, c.n_experts, div,
+                                            c.T, A, row_vec, (uint4*)x_perm, status);
   count_launch(lc);
   return cudaGetLastError();
 }

@@ -25,7 +25,7 @@ struct SimtArgs {
   const void* bs1;         // shared up
   void* out_routed;        // [A, N]
   void* out_shared;        // [T, N_s]
-  int E, T, k, K, N, K_s, N_s;
+  int E, T, rows_cap, K, N, K_s, N_s;   // rows_cap: rows of the grouped buffers
   int has_shared;
 };
 
@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(256) experts_simt_kernel(SimtArgs p) {
   const TIn *A, *B0, *B1;
   if (!shared) {
     // clamp caller-provided offsets to the grouped buffer [0, A)
-    const int n_assign = p.T * p.k;
+    const int n_assign = p.rows_cap;
     row0 = min(max(p.offsets[g], 0), n_assign);
     rows = min(max(p.offsets[g + 1], row0), n_assign) - row0;
     K = p.K;
@@ -134,7 +134,7 @@ cudaError_t run(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s) {
   SimtArgs p{};
   p.E = E;
   p.T = T;
-  p.k = c.top_k;
+  p.rows_cap = a.rows > 0 ? a.rows : T * c.top_k;
   p.offsets = a.offsets;
   p.has_shared = has_shared;
   // gate/up + SwiGLU: [rows, d] x [F, d]^T -> h [rows, F]

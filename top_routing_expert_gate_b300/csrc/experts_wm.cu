@@ -490,7 +490,7 @@ cudaError_t launch_gemm_wm(const moe_config_t& c, const ExpertArgs& a, int which
                            cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
   const int T = c.T, E = c.n_experts, d = c.d_model, F = c.d_ff, Fs = c.d_ff_shared;
-  const int A = T * c.top_k;
+  const int A = a.rows > 0 ? a.rows : T * c.top_k;
   const bool has_shared = Fs > 0 && a.ws_gate != nullptr;
 
   WmParams p1{};

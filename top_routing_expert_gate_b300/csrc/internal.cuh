@@ -51,11 +51,28 @@ struct WsLayout {
   size_t y_perm;      // [A, d] fp32
   size_t y_shared;    // [T, d] fp32
   size_t shared_w;    // [T] fp32, per-token shared-expert gate
+  size_t ec_scores;   // [E, T] fp32 (expert choice)
+  size_t ec_w;        // [E, C] fp32 (expert choice)
+  size_t ec_rowmap;   // [T, E] int32 (expert choice)
   size_t total;
   int nb;             // dispatch blocks
 };
 
 WsLayout ws_layout(const moe_config_t& c);
+
+// Tokens each expert takes under expert-choice routing (at most T).
+inline int ec_capacity(const moe_config_t& c) {
+  long long C = c.capacity >= 0 ? (long long)c.capacity
+                                : ((long long)c.T * c.top_k + c.n_experts - 1) / c.n_experts;
+  if (C > c.T) C = c.T;
+  return (int)C;
+}
+// Rows of the grouped (expert-major) buffers x_perm, h, y_perm and perm.
+inline size_t grouped_rows(const moe_config_t& c) {
+  if (c.routing == MOE_ROUTE_EXPERT_CHOICE) return (size_t)c.n_experts * (size_t)ec_capacity(c);
+  return (size_t)c.T * (size_t)c.top_k;
+}
+constexpr int kEcMaxTokens = 32768;   // expert choice keeps one score column in shared memory
 
 inline size_t act_bytes(const moe_config_t& c) { return c.act_dtype == MOE_BF16 ? 2 : 4; }
 
@@ -133,10 +150,27 @@ cudaError_t launch_dispatch(const moe_config_t& c, const int32_t* idx, int32_t* 
                             uint8_t* drop_mask, int32_t* status, cudaStream_t s,
                             LaunchCounter* lc = nullptr);
 
-// x_perm[r] = x[perm[r] / k] for r < offsets[E].
+// x_perm[r] = x[perm[r] / div] for r < offsets[E] (div = top_k: perm holds
+// assignment ids; 1: perm holds tokens).
 cudaError_t launch_gather(const moe_config_t& c, const void* x, const int32_t* perm,
                           const int32_t* offsets, void* x_perm, int32_t* status,
-                          cudaStream_t s, LaunchCounter* lc = nullptr);
+                          cudaStream_t s, LaunchCounter* lc = nullptr, int div = 0);
+
+// Expert choice: scores, per-expert top-C selection (tokens / weights [E, C],
+// offsets e*C, counts C, drops 0) and the mean probability.
+// rowmap [T, E] (nullable): row of (t, e) in the grouped buffers, -1 if e did not take t.
+cudaError_t launch_ec_route(const moe_config_t& c, const LogitsView& z, float* scores_t,
+                            float* mp_partial, float* mean_prob, int32_t* tokens, float* weights,
+                            int32_t* rowmap, int32_t* offsets, int32_t* counts, int32_t* drops,
+                            cudaStream_t s, LaunchCounter* lc = nullptr);
+// y[t] = sum over experts e that took t (ascending e) of w * y_perm[row] (+ w_s[t] y_shared[t]).
+cudaError_t launch_ec_combine(const moe_config_t& c, const float* y_perm, const int32_t* rowmap,
+                              const float* weights, const float* y_shared, const float* shared_w,
+                              void* y, int32_t* status, cudaStream_t s,
+                              LaunchCounter* lc = nullptr);
+// mean_prob[e] = sum of the per-block partials / T (fixed order).
+cudaError_t launch_mean_prob_finalize(const float* mp_partial, int nblocks, int E, int T,
+                                      float* mean_prob, cudaStream_t s, LaunchCounter* lc);
 
 // row_of[perm[r]] = r for r < offsets[E] (row_of pre-filled with -1).
 cudaError_t launch_invert_perm(const moe_config_t& c, const int32_t* perm,
@@ -164,6 +198,7 @@ struct ExpertArgs {
   float* y_shared;      // [T, d]
   int32_t* status;
   const moe_weight_scales_t* scales = nullptr;   // E4M3 weights only
+  int rows = 0;                                  // grouped rows (0: T * top_k)
   cudaEvent_t ev_up = nullptr;     // recorded before the gate/up GEMM when set (fp32 path)
   cudaEvent_t ev_down = nullptr;   // recorded before the down GEMM when set (fp32 path)
   LaunchCounter* launches = nullptr;

@@ -15,6 +15,8 @@ WsLayout ws_layout(const moe_config_t& c) {
   const size_t T = (size_t)c.T, E = (size_t)c.n_experts, k = (size_t)c.top_k;
   const size_t d = (size_t)c.d_model, F = (size_t)c.d_ff, Fs = (size_t)c.d_ff_shared;
   const size_t A = T * k;
+  const size_t R = grouped_rows(c);   // rows of the expert-major buffers
+  const bool ec = c.routing == MOE_ROUTE_EXPERT_CHOICE;
   const size_t ab = act_bytes(c);
   L.nb = (int)((A + kDispatchChunk - 1) / kDispatchChunk);
   size_t o = 0;
@@ -34,15 +36,18 @@ WsLayout ws_layout(const moe_config_t& c) {
   L.mean_prob = take(E * 4);
   L.block_hist = take((size_t)L.nb * E * 4);
   L.block_base = take((size_t)L.nb * E * 4);
-  L.perm = take(A * 4);
+  L.perm = take(R * 4);
   L.row_of = take(A * 4);
   L.drop_mask = take(A);
-  L.x_perm = take(A * d * ab);
-  L.h = take(A * F * ab);
+  L.x_perm = take(R * d * ab);
+  L.h = take(R * F * ab);
   L.h_shared = take(T * Fs * ab);
-  L.y_perm = take(A * d * 4);
+  L.y_perm = take(R * d * 4);
   L.y_shared = take(T * d * 4);
   L.shared_w = take(T * 4);
+  L.ec_scores = take(ec ? E * T * 4 : 0);
+  L.ec_w = take(ec ? R * 4 : 0);
+  L.ec_rowmap = take(ec ? T * E * 4 : 0);
   L.total = o;
   return L;
 }
@@ -81,6 +86,13 @@ moe_status_t check_config(const moe_config_t* c) {
   }
   if (c->weight_format != MOE_WEIGHTS_ACT && c->weight_format != MOE_WEIGHTS_FP8_E4M3)
     return MOE_ERR_INVALID_ARG;
+  if (c->routing != MOE_ROUTE_TOKEN_CHOICE && c->routing != MOE_ROUTE_EXPERT_CHOICE)
+    return MOE_ERR_INVALID_ARG;
+  if (c->routing == MOE_ROUTE_EXPERT_CHOICE) {
+    if (c->n_group > 1) return MOE_ERR_INVALID_ARG;
+    if (c->T > kEcMaxTokens) return MOE_ERR_UNSUPPORTED;
+    if ((long long)c->n_experts * ec_capacity(*c) > 0x3fffffffLL) return MOE_ERR_INVALID_ARG;
+  }
   if (c->weight_format == MOE_WEIGHTS_FP8_E4M3 && c->act_dtype != MOE_BF16)
     return MOE_ERR_UNSUPPORTED;
   // expert groups: 0 or 1 = none; otherwise equal groups of at least two
@@ -184,7 +196,7 @@ moe_status_t check_shared_args(const moe_config_t* c, const void* g, const void*
 
 extern "C" {
 
-int32_t moe_version(void) { return 300; }
+int32_t moe_version(void) { return 400; }
 
 const char* moe_status_string(moe_status_t st) {
   switch (st) {
@@ -206,6 +218,11 @@ int32_t moe_capacity(int32_t T, int32_t E, double capacity_factor) {
   return (int32_t)c;
 }
 
+int32_t moe_expert_choice_capacity(const moe_config_t* cfg) {
+  if (check_config(cfg) != MOE_OK) return -1;
+  return ec_capacity(*cfg);
+}
+
 moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes) {
   MOE_TRY(check_config(cfg));
   if (!bytes) return MOE_ERR_INVALID_ARG;
@@ -225,6 +242,7 @@ moe_status_t moe_topk_from_logits(const moe_config_t* cfg, const float* logits,
                                   const float* score_bias, int32_t* topk_idx, float* topk_w,
                                   float* mean_prob, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(check_config(cfg));
+  if (cfg->routing != MOE_ROUTE_TOKEN_CHOICE) return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_ws(cfg, ws, ws_bytes));
   if (bad_ptr(cfg, logits) || bad_ptr(cfg, topk_idx) || bad_ptr(cfg, topk_w) ||
       bad_opt(mean_prob) || bad_opt(score_bias))
@@ -233,6 +251,24 @@ moe_status_t moe_topk_from_logits(const moe_config_t* cfg, const float* logits,
   const LogitsView view{logits, 1, 0, nullptr};
   return cuda_status(launch_topk(*cfg, view, score_bias, nullptr, topk_idx, topk_w,
                                  at<float>(ws, L.mp_partial), mean_prob, (cudaStream_t)stream));
+}
+
+moe_status_t moe_expert_choice_from_logits(const moe_config_t* cfg, const float* logits,
+                                           int32_t* tokens, float* weights, float* mean_prob,
+                                           void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_TRY(check_ws(cfg, ws, ws_bytes));
+  if (cfg->routing != MOE_ROUTE_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
+  if (bad_ptr(cfg, logits) || bad_opt(mean_prob) ||
+      (ec_capacity(*cfg) > 0 && (bad_ptr(cfg, tokens) || bad_ptr(cfg, weights))))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*cfg);
+  const LogitsView view{logits, 1, 0, nullptr};
+  return cuda_status(launch_ec_route(*cfg, view, at<float>(ws, L.ec_scores),
+                                     at<float>(ws, L.mp_partial), mean_prob, tokens, weights,
+                                     nullptr, at<int32_t>(ws, L.offsets),
+                                     at<int32_t>(ws, L.counts), at<int32_t>(ws, L.drops),
+                                     (cudaStream_t)stream));
 }
 
 moe_status_t moe_update_score_bias(const moe_config_t* cfg, const int32_t* counts,
@@ -251,6 +287,7 @@ moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x, const void*
                              float* logits_out, int32_t* topk_idx, float* topk_w,
                              float* mean_prob, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(check_config(cfg));
+  if (cfg->routing != MOE_ROUTE_TOKEN_CHOICE) return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_ws(cfg, ws, ws_bytes));
   if (bad_ptr(cfg, x) || bad_ptr(cfg, w_router) || bad_ptr(cfg, topk_idx) ||
       bad_ptr(cfg, topk_w) || bad_opt(router_bias) || bad_opt(score_bias) ||
@@ -270,6 +307,7 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* topk_idx, int3
                           int32_t* drops, int32_t* offsets, int32_t* perm, uint8_t* drop_mask,
                           void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(check_config(cfg));
+  if (cfg->routing != MOE_ROUTE_TOKEN_CHOICE) return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_ws(cfg, ws, ws_bytes));
   if (bad_ptr(cfg, topk_idx) || bad_ptr(cfg, perm) || bad_ptr(cfg, drop_mask) || !counts ||
       !drops || !offsets || !aligned16(counts) || !aligned16(drops) || !aligned16(offsets))
@@ -318,6 +356,7 @@ moe_status_t moe_grouped_swiglu(const moe_config_t* cfg, const void* x, const in
   a.y_shared = y_shared;
   a.status = status;
   a.scales = scales;
+  a.rows = (int)grouped_rows(*cfg);
   return cuda_status(run_experts(*cfg, a, s));
 }
 
@@ -327,6 +366,7 @@ moe_status_t moe_combine(const moe_config_t* cfg, const float* y_perm, const flo
                          const float* shared_weight, void* y, void* ws, size_t ws_bytes,
                          void* stream) {
   MOE_TRY(check_config(cfg));
+  if (cfg->routing != MOE_ROUTE_TOKEN_CHOICE) return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_ws(cfg, ws, ws_bytes));
   if (bad_ptr(cfg, y_perm) || bad_ptr(cfg, topk_w) || bad_ptr(cfg, perm) ||
       bad_ptr(cfg, drop_mask) || bad_ptr(cfg, y) || !offsets || !aligned16(offsets) ||
@@ -387,6 +427,8 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
   MOE_TRY(check_shared_args(cfg, ws_gate, ws_up, ws_down));
   if (bad_opt(shared_gate) || (shared_gate && !ws_gate)) return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_scales(cfg, scales, ws_gate != nullptr));
+  const bool ec = cfg->routing == MOE_ROUTE_EXPERT_CHOICE;
+  if (ec && (topk_idx || topk_w || score_bias)) return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(*cfg);
   cudaStream_t s = (cudaStream_t)stream;
   const moe_config_t& c = *cfg;
@@ -419,12 +461,22 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
   float* shared_w = shared_gate ? at<float>(ws, L.shared_w) : nullptr;
   if (shared_gate) MOE_TRY_CUDA(launch_shared_gate(c, x, shared_gate, shared_w, s, &lc));
   MOE_TRY_CUDA(mark(MOE_STAGE_TOPK));
-  MOE_TRY_CUDA(launch_topk(c, view, score_bias, nullptr, idx, g, at<float>(ws, L.mp_partial),
-                           mean_prob, s, &lc));
-  MOE_TRY_CUDA(mark(MOE_STAGE_DISPATCH));
-  MOE_TRY_CUDA(launch_dispatch(c, idx, at<int32_t>(ws, L.block_hist),
-                               at<int32_t>(ws, L.block_base), cnt, drp, offsets, perm, row_of,
-                               dmask, status, s, &lc));
+  float* ec_w = at<float>(ws, L.ec_w);
+  if (ec) {
+    // expert choice: scores and the per-expert selection give perm (tokens,
+    // expert-major, ascending), the weights and offsets e*C directly
+    MOE_TRY_CUDA(launch_ec_route(c, view, at<float>(ws, L.ec_scores), at<float>(ws, L.mp_partial),
+                                 mean_prob, perm, ec_w, at<int32_t>(ws, L.ec_rowmap), offsets, cnt,
+                                 drp, s, &lc));
+    MOE_TRY_CUDA(mark(MOE_STAGE_DISPATCH));
+  } else {
+    MOE_TRY_CUDA(launch_topk(c, view, score_bias, nullptr, idx, g, at<float>(ws, L.mp_partial),
+                             mean_prob, s, &lc));
+    MOE_TRY_CUDA(mark(MOE_STAGE_DISPATCH));
+    MOE_TRY_CUDA(launch_dispatch(c, idx, at<int32_t>(ws, L.block_hist),
+                                 at<int32_t>(ws, L.block_base), cnt, drp, offsets, perm, row_of,
+                                 dmask, status, s, &lc));
+  }
   MOE_TRY_CUDA(mark(MOE_STAGE_GATHER));
   void* x_perm = at<char>(ws, L.x_perm);
   MOE_TRY_CUDA(launch_gather(c, x, perm, offsets, x_perm, status, s, &lc));
@@ -445,13 +497,18 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
   a.y_shared = has_shared ? at<float>(ws, L.y_shared) : nullptr;
   a.status = status;
   a.scales = scales;
+  a.rows = (int)grouped_rows(c);
   a.ev_up = ev ? ev[MOE_STAGE_GATE_UP] : nullptr;
   a.ev_down = ev ? ev[MOE_STAGE_DOWN] : nullptr;
   a.launches = &lc;
   MOE_TRY_CUDA(run_experts(c, a, s));
   MOE_TRY_CUDA(mark(MOE_STAGE_COMBINE));
-  MOE_TRY_CUDA(
-      launch_combine(c, a.y_perm, g, row_of, dmask, a.y_shared, shared_w, y, status, s, &lc));
+  if (ec)
+    MOE_TRY_CUDA(launch_ec_combine(c, a.y_perm, at<int32_t>(ws, L.ec_rowmap), ec_w, a.y_shared,
+                                   shared_w, y, status, s, &lc));
+  else
+    MOE_TRY_CUDA(
+        launch_combine(c, a.y_perm, g, row_of, dmask, a.y_shared, shared_w, y, status, s, &lc));
   MOE_TRY_CUDA(mark(MOE_NUM_STAGES));
   if (n_launches) *n_launches = lc.n;
   return MOE_OK;

@@ -369,6 +369,13 @@ cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_ro
   return cudaGetLastError();
 }
 
+cudaError_t launch_mean_prob_finalize(const float* mp_partial, int nblocks, int E, int T,
+                                      float* mean_prob, cudaStream_t s, LaunchCounter* lc) {
+  mean_prob_finalize_kernel<<<(E + 255) / 256, 256, 0, s>>>(mp_partial, nblocks, E, T, mean_prob);
+  count_launch(lc);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_score_bias_update(const moe_config_t& c, const int32_t* counts,
                                      const int32_t* drops, float gamma, float* bias,
                                      cudaStream_t s) {

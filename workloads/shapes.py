@@ -51,6 +51,7 @@ class MoEShape:
     score_bias_std: Optional[float] = None   # selection-only score bias ~ N(0, std^2)
     shared_gate: bool = False         # per-token sigmoid gate on the shared expert
     weight_format: str = "act"        # "act" (weights in dtype) or "fp8" (E4M3 + row scales)
+    routing: str = "token"            # "token" (top-k per token) or "expert" (top-C per expert)
 
     def with_tokens(self, T: int) -> "MoEShape":
         return replace(self, T=T)
@@ -82,6 +83,13 @@ SHAPES = {
     "dsv3_decode": MoEShape("dsv3_decode", T=64, d=7168, E=256, k=8, F=2048,
                             F_s=2048, gate="sigmoid", renormalize=True, rsf=2.5,
                             capacity_factor=None, zipf_s=None, dtype="bf16"),
+    # the Switch-shaped layer routed by expert choice: each expert takes
+    # C = T * k / E = 256 tokens ("MoE 路由为什么是最难的部分": each expert takes the
+    # fixed number of tokens it wants most)
+    "switch_expert_choice": MoEShape("switch_expert_choice", T=16384, d=2048, E=64, k=1,
+                                     F=8192, F_s=0, gate="softmax", renormalize=False, rsf=1.0,
+                                     capacity_factor=None, zipf_s=None, dtype="bf16",
+                                     routing="expert"),
     # the same layers with E4M3 expert weights (one scale per output channel)
     "dsv3_decode_fp8": MoEShape("dsv3_decode_fp8", T=64, d=7168, E=256, k=8, F=2048,
                                 F_s=2048, gate="sigmoid", renormalize=True, rsf=2.5,
