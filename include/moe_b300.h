@@ -82,10 +82,10 @@ typedef enum { MOE_BF16 = 0, MOE_FP32 = 1 } moe_dtype_t;
  * fp32 accumulator of each output. */
 typedef enum { MOE_WEIGHTS_ACT = 0, MOE_WEIGHTS_FP8_E4M3 = 1 } moe_weight_format_t;
 /* Who chooses.  MOE_ROUTE_TOKEN_CHOICE: each token takes its top_k experts
- * (selection rule below).  MOE_ROUTE_EXPERT_CHOICE ("MoE 路由为什么是最难的
- * 部分", the routing article: each expert takes the fixed number of tokens it
- * wants most, which balances the load by construction; a token may be taken
- * by no expert): expert e takes the C = moe_expert_choice_capacity(cfg)
+ * (selection rule below).  MOE_ROUTE_EXPERT_CHOICE (the amazingdata.cn
+ * article on MoE routing, paragraph on expert choice: each expert takes a
+ * fixed number of the tokens it scores highest, which balances the load by
+ * construction; a token may be taken by no expert): expert e takes the C = moe_expert_choice_capacity(cfg)
  * tokens with the largest fp32 score s[t, e] (ties to the lower token), and
  * y_t = sum over the experts that took t of s[t, e] * E_e(x_t) (+ shared). */
 typedef enum { MOE_ROUTE_TOKEN_CHOICE = 0, MOE_ROUTE_EXPERT_CHOICE = 1 } moe_routing_t;

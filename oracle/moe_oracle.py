@@ -111,8 +111,8 @@ def topk_weights(scores: np.ndarray, idx: np.ndarray, renormalize: bool,
                  routed_scaling_factor: float = 1.0) -> np.ndarray:
     """Combine weights g[t,j] of the chosen experts.
 
-    With renormalisation ([moe10] top-k section: "再在两者之间归一化"; the
-    block sketch's `w / w.sum(-1)`): g_j = score_j / sum_sel score, then
+    With renormalisation ([moe10] top-k section, whose worked example divides
+    the two chosen scores by their sum; the block sketch's `w / w.sum(-1)`): g_j = score_j / sum_sel score, then
     multiplied by routed_scaling_factor (DeepSeek-V3: 2.5).  Without it
     ([explain] "门控是怎么挑专家的": out = sum score_i * expert_i): g_j = score_j
     (times the factor, which is 1 for the configurations that skip renorm).
@@ -185,15 +185,15 @@ def topk_experts_biased(scores: np.ndarray, score_bias: Optional[np.ndarray], k:
 
 def update_score_bias(score_bias: np.ndarray, load: np.ndarray, gamma: float) -> np.ndarray:
     """One bias step after a batch: an expert above the mean load loses gamma,
-    one below it gains gamma ([moe10]: "超载的专家 b_i 减 γ，不足的加 γ");
+    one below it gains gamma ([moe10] "DeepSeek-V3 的无辅助损失偏置");
     an expert exactly at the mean is left unchanged."""
     load = np.asarray(load, dtype=np.float64)
     return np.asarray(score_bias, dtype=np.float64) - gamma * np.sign(load - np.mean(load))
 
 
 # ---------------------------------------------------------------------------
-# Expert-choice routing ([routing]: "让每个专家挑走它最想要的固定数量 token" -
-# each expert takes the fixed number of tokens it wants most, which balances
+# Expert-choice routing ([routing], the paragraph on expert choice: each
+# expert takes a fixed number of the tokens it scores highest, which balances
 # the load by construction; a token may be taken by no expert).
 # ---------------------------------------------------------------------------
 

@@ -1,6 +1,6 @@
-"""GPU parity of expert-choice routing ("MoE 路由为什么是最难的部分": each
-expert takes the fixed number of tokens it wants most; a token may be taken
-by no expert).
+"""GPU parity of expert-choice routing (the amazingdata.cn article on MoE
+routing, paragraph on expert choice: each expert takes a fixed number of the
+tokens it scores highest; a token may be taken by no expert).
 
 Fed the same fp32 logits, each expert's chosen tokens must equal the
 oracle's whenever its C-th and (C+1)-th largest scores are separated by

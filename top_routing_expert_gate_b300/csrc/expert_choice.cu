@@ -1,7 +1,7 @@
-// Expert-choice routing: each expert takes the fixed number of tokens it
-// wants most ("MoE 路由为什么是最难的部分", the routing article: "让每个专家
-// 挑走它最想要的固定数量 token"; the load is balanced by construction and a
-// token may be taken by no expert).
+// Expert-choice routing: each expert takes a fixed number of the tokens it
+// scores highest (the amazingdata.cn article on MoE routing, paragraph on
+// expert choice; the load is balanced by construction and a token may be
+// taken by no expert).
 //
 //   scores   s[t, e] = softmax_e(z[t, :]) or sigmoid(z[t, e])  (fp32)
 //   select   expert e takes the C tokens with the largest s[t, e], ties to

@@ -17,6 +17,9 @@ Each shape follows a model configuration that the pages describe:
 * ``dsv3_decode_fp8`` / ``dsv3_prefill_fp8`` - the DeepSeek-V3 layers with the
   expert weights stored as FP8 E4M3 codes and one scale per output channel
   (same page, "推理时": DeepSeek-V3 ships FP8 weights).
+* ``switch_expert_choice`` - the Switch-shaped layer routed by expert choice:
+  each of the 64 experts takes the 256 tokens it scores highest (the
+  amazingdata.cn article on MoE routing, paragraph on expert choice).
 * ``switch`` - a Switch-Transformer-style top-1 layer with an expert capacity
   of ceil(T/E x 1.25) and token dropping (same page, section
   "负载不均：路由坍缩与丢 token"), with a Zipf-skewed router bias so that the
@@ -84,8 +87,8 @@ SHAPES = {
                             F_s=2048, gate="sigmoid", renormalize=True, rsf=2.5,
                             capacity_factor=None, zipf_s=None, dtype="bf16"),
     # the Switch-shaped layer routed by expert choice: each expert takes
-    # C = T * k / E = 256 tokens ("MoE 路由为什么是最难的部分": each expert takes the
-    # fixed number of tokens it wants most)
+    # C = T * k / E = 256 tokens (the amazingdata.cn routing article, paragraph
+    # on expert choice: each expert takes a fixed number of its best tokens)
     "switch_expert_choice": MoEShape("switch_expert_choice", T=16384, d=2048, E=64, k=1,
                                      F=8192, F_s=0, gate="softmax", renormalize=False, rsf=1.0,
                                      capacity_factor=None, zipf_s=None, dtype="bf16",
