@@ -92,6 +92,7 @@ def load_peaks():
 
 # Sources of the grouped GEMM kernels whose DRAM counters profiles/traffic.json stores.
 GEMM_SOURCES = ("experts_tc.cu", "tc_common.cuh")
+E2E_PIPELINE = 2   # batches in flight in the end-to-end leg
 
 
 def source_digest() -> str:
@@ -426,25 +427,42 @@ def main(argv=None):
         vals = [ev[si].elapsed_time(ev[si + 1]) for ev in step_events]
         stage_ms[name] = sum(vals) / len(vals)
 
-    # end to end through the public API: pinned host x in, y out, every step
-    x_host = x.cpu().pin_memory()
-    y_host = torch.empty((T, d), dtype=torch.float32).pin_memory()
-    x_dev = torch.empty_like(x)
+    # end to end through the C ABI's host-buffer call: every step copies its
+    # x from pinned host memory, runs the layer and copies y back.  Two
+    # batches are in flight on two streams (each with its own staging buffers
+    # and workspace), so that one batch's copies overlap the other's kernels.
+    n_pipe = E2E_PIPELINE
+    pipes = []
+    for j in range(n_pipe):
+        pipes.append({"stream": torch.cuda.Stream(dev), "x_host": x.cpu().pin_memory(),
+                      "y_host": torch.empty((T, d), dtype=y.dtype).pin_memory(),
+                      "x": torch.empty_like(x), "y": torch.empty_like(y),
+                      "ws": ws if j == 0 else moe.Workspace(cfg, dev)})
+
+    def e2e_step(i):
+        p = pipes[i % n_pipe]
+        moe.layer_forward_host(cfg, p["x_host"], w, p["ws"], p["x"], p["y"], p["y_host"],
+                               stream=p["stream"])
+
     e2e_start = torch.cuda.Event(enable_timing=True)
     e2e_end = torch.cuda.Event(enable_timing=True)
-    for _ in range(2):
-        x_dev.copy_(x_host, non_blocking=True)
-        moe.layer_forward(cfg, x_dev, w, ws=ws, y=y, stats=False)
-        y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    for i in range(2 * n_pipe):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
     e2e_start.record(stream)
-    for _ in range(args.e2e_steps):
-        x_dev.copy_(x_host, non_blocking=True)
-        moe.layer_forward(cfg, x_dev, w, ws=ws, y=y, stats=False)
-        y_host.copy_(y, non_blocking=True)
+    for p in pipes:
+        p["stream"].wait_event(e2e_start)
+    for i in range(args.e2e_steps):
+        e2e_step(i)
+    for p in pipes:
+        stream.wait_stream(p["stream"])
     e2e_end.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e2e_start.elapsed_time(e2e_end) / args.e2e_steps, dev)
+    for p in pipes[1:]:
+        if moe.moe_get_error(p["ws"]) != 0:
+            raise RuntimeError("device status after the end-to-end steps")
 
     if rank != 0:
         if world > 1:
@@ -501,7 +519,8 @@ def main(argv=None):
         "clocks": clk,
         "e2e": {"value": tokens_per_second(T, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": x.numel() * x.element_size(),
-                "d2h_bytes_per_step": y.numel() * y.element_size()},
+                "d2h_bytes_per_step": y.numel() * y.element_size(),
+                "api": "moe_layer_forward_host", "batches_in_flight": E2E_PIPELINE},
     }
     if world == 1 and not args.no_cpu_baseline:
         times = time_oracle(shape, inputs, args.cpu_sample_tokens, args.cpu_steps)

@@ -332,6 +332,28 @@ MOE_API moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, c
                                int32_t* counts, int32_t* drops, float* mean_prob,
                                void* ws, size_t ws_bytes, void* stream);
 
+/* moe_layer_forward with the token rows in host memory: enqueues, on
+ * `stream`, the copy of x_host [T, d_model] (act_dtype) into the device
+ * buffer x, the layer forward of x into the device buffer y, and the copy of
+ * y into y_host [T, d_model] (out_dtype).  x and y are caller-owned device
+ * staging buffers with the layout of moe_layer_forward; every other argument
+ * is as there.  The copies are asynchronous when x_host and y_host are
+ * page-locked (cudaHostAlloc or cudaHostRegister); y_host is complete once
+ * `stream` has reached this call's end.  Callers that keep two batches in
+ * flight on two streams (each with its own staging buffers and workspace)
+ * overlap one batch's copies with the other's kernels.  Argument errors are
+ * returned before anything is enqueued; a failed copy returns MOE_ERR_CUDA. */
+MOE_API moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* x_host, void* x,
+                                            const void* w_router, const float* router_bias,
+                                            const float* score_bias, const void* w_gate,
+                                            const void* w_up, const void* w_down,
+                                            const void* ws_gate, const void* ws_up,
+                                            const void* ws_down, const void* shared_gate,
+                                            const moe_weight_scales_t* scales, void* y,
+                                            void* y_host, int32_t* topk_idx, float* topk_w,
+                                            int32_t* counts, int32_t* drops, float* mean_prob,
+                                            void* ws, size_t ws_bytes, void* stream);
+
 /* Stages of moe_layer_forward, in launch order (for moe_layer_forward_profiled). */
 typedef enum {
   MOE_STAGE_ROUTER = 0,    /* router logits                                  */

@@ -159,6 +159,13 @@ def test_entry_points_reject_missing_workspace_and_pointers():
                                  None, None, None, None, ctypes.byref(sc_ok), fake, None, None,
                                  None, None, None, fake, need, None) == B.MOE_ERR_INVALID_ARG
     assert _ws_size(_cfg(act_dtype="fp32", weight_format="fp8"))[0] == B.MOE_ERR_UNSUPPORTED
+    # host-buffer call: null host x or host y
+    assert lib.moe_layer_forward_host(ctypes.byref(cfg), None, fake, fake, None, None, fake, fake,
+                                      fake, None, None, None, None, None, fake, fake, None, None,
+                                      None, None, None, fake, need, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_forward_host(ctypes.byref(cfg), fake, fake, fake, None, None, fake, fake,
+                                      fake, None, None, None, None, None, fake, None, None, None,
+                                      None, None, None, fake, need, None) == B.MOE_ERR_INVALID_ARG
     # null config
     assert lib.moe_layer_forward(None, fake, fake, None, None, fake, fake, fake, None, None, None,
                                  None, None, fake, None, None, None, None, None, fake, need,

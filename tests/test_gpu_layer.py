@@ -171,6 +171,41 @@ def test_deterministic_and_split_calls_match_fused():
     assert moe.moe_get_error(ws) == 0
 
 
+@pytest.mark.parametrize("out_dtype", ["fp32", "bf16"])
+def test_host_buffer_call_matches_device_call(out_dtype):
+    # the host-buffer entry point: x copied in, the layer, y copied out, on
+    # two streams with their own staging buffers and workspaces
+    s = MID_SHAPES["mid_sigmoid_shared"]
+    inp = make_inputs(s, device=DEV, seed=16)
+    cfg = moe.config_from_shape(s, out_dtype=out_dtype)
+    w = moe.LayerWeights.from_inputs(inp)
+    ref = moe.layer_forward(cfg, inp["x"], w)["y"].cpu()
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    outs = []
+    for j in range(4):
+        st = streams[j % 2]
+        x_host = inp["x"].cpu().pin_memory()
+        y_host = torch.full(ref.shape, float("nan"), dtype=ref.dtype).pin_memory()
+        x_dev = torch.empty_like(inp["x"])
+        y_dev = torch.empty(ref.shape, dtype=ref.dtype, device=DEV)
+        ws = moe.Workspace(cfg)
+        torch.cuda.synchronize()
+        moe.layer_forward_host(cfg, x_host, w, ws, x_dev, y_dev, y_host, stream=st)
+        outs.append((y_host, ws))
+    torch.cuda.synchronize()
+    for y_host, ws in outs:
+        assert moe.moe_get_error(ws) == 0
+        assert torch.equal(y_host, ref)
+    # an empty batch copies nothing
+    c0 = moe.config_from_shape(_shape(T=0))
+    e = torch.empty((0, s.d), dtype=torch.float32)
+    moe.layer_forward_host(c0, e, moe.LayerWeights.from_inputs(make_inputs(_shape(T=1), device=DEV,
+                                                                           seed=5)),
+                           moe.Workspace(c0), torch.empty((0, s.d), device=DEV),
+                           torch.empty((0, s.d), device=DEV), e)
+    torch.cuda.synchronize()
+
+
 def test_gated_shared_expert_split_calls_match_fused():
     s = MID_SHAPES["mid_gated_shared"]
     inp = make_inputs(s, device=DEV, seed=7)

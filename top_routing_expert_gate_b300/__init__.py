@@ -11,5 +11,6 @@ from .api import (  # noqa: F401
     moe_layer_forward, moe_layer_forward_profiled, moe_router_topk, moe_topk_from_logits,
     moe_update_score_bias, moe_version, moe_workspace_size, route, topk_from_logits,
     moe_shared_gate_weights, moe_balance_loss, moe_expert_choice_capacity,
-    moe_expert_choice_from_logits, expert_choice_from_logits,
+    moe_expert_choice_from_logits, expert_choice_from_logits, layer_forward_host,
+    moe_layer_forward_host,
 )

@@ -229,6 +229,28 @@ def moe_layer_forward(cfg, x, w_router, router_bias, score_bias, w_gate, w_up, w
         ws.nbytes, _stream(stream)), "moe_layer_forward")
 
 
+def _host_ptr(t: torch.Tensor, name: str, dtype: torch.dtype, numel: int):
+    if t.is_cuda or not t.is_contiguous() or t.dtype != dtype or t.numel() != numel:
+        raise ValueError(f"{name} must be a contiguous host tensor of {numel} {dtype}")
+    return t.data_ptr()
+
+
+def moe_layer_forward_host(cfg, x_host, x, w_router, router_bias, score_bias, w_gate, w_up,
+                           w_down, ws_gate, ws_up, ws_down, shared_gate, scales, y, y_host,
+                           topk_idx, topk_w, counts, drops, mean_prob, ws: Workspace,
+                           stream=None) -> None:
+    """moe_layer_forward with x read from and y written to host tensors (the
+    copies run on ``stream``; pin both for them to be asynchronous)."""
+    n = cfg.T * cfg.d_model
+    check(load_library().moe_layer_forward_host(
+        ctypes.byref(cfg), _host_ptr(x_host, "x_host", x.dtype, n), _ptr(x), _ptr(w_router),
+        _ptr(router_bias), _ptr(score_bias), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+        _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), _ptr(shared_gate), _scales_ref(scales),
+        _ptr(y), _host_ptr(y_host, "y_host", y.dtype, n), _ptr(topk_idx), _ptr(topk_w),
+        _ptr(counts), _ptr(drops), _ptr(mean_prob), ws.ptr, ws.nbytes, _stream(stream)),
+        "moe_layer_forward_host")
+
+
 def moe_layer_forward_profiled(cfg, x, w_router, router_bias, score_bias, w_gate, w_up, w_down,
                                ws_gate, ws_up, ws_down, shared_gate, scales, y, topk_idx, topk_w,
                                counts, drops, mean_prob, ws: Workspace, stage_events,
@@ -324,6 +346,19 @@ class LayerWeights:
                    inputs.get("router_bias"), inputs.get("ws_gate"), inputs.get("ws_up"),
                    inputs.get("ws_down"), inputs.get("score_bias"), inputs.get("shared_gate"),
                    WeightScales.from_inputs(inputs))
+
+
+def layer_forward_host(cfg, x_host: torch.Tensor, w: LayerWeights, ws: Workspace,
+                       x: torch.Tensor, y: torch.Tensor, y_host: torch.Tensor,
+                       stream=None) -> torch.Tensor:
+    """One layer call on host token rows: x_host is copied into the device
+    staging buffer x, the layer writes y, and y is copied into y_host, all
+    enqueued on ``stream``; y_host is valid once the stream has reached the
+    end of the call.  Statistics are not returned."""
+    moe_layer_forward_host(cfg, x_host, x, w.w_router, w.router_bias, w.score_bias, w.w_gate,
+                           w.w_up, w.w_down, w.ws_gate, w.ws_up, w.ws_down, w.shared_gate,
+                           w.scales, y, y_host, None, None, None, None, None, ws, stream)
+    return y_host
 
 
 def layer_forward(cfg, x, w: LayerWeights, ws: Optional[Workspace] = None,

@@ -532,6 +532,31 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
                             counts, drops, mean_prob, ws, ws_bytes, stream, nullptr, nullptr);
 }
 
+moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* x_host, void* x,
+                                    const void* w_router, const float* router_bias,
+                                    const float* score_bias, const void* w_gate,
+                                    const void* w_up, const void* w_down, const void* ws_gate,
+                                    const void* ws_up, const void* ws_down,
+                                    const void* shared_gate, const moe_weight_scales_t* scales,
+                                    void* y, void* y_host, int32_t* topk_idx, float* topk_w,
+                                    int32_t* counts, int32_t* drops, float* mean_prob, void* ws,
+                                    size_t ws_bytes, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_TRY(check_ws(cfg, ws, ws_bytes));
+  if (cfg->T > 0 && (x_host == nullptr || y_host == nullptr || bad_ptr(cfg, x) || bad_ptr(cfg, y)))
+    return MOE_ERR_INVALID_ARG;
+  const cudaStream_t s = (cudaStream_t)stream;
+  const size_t n = (size_t)cfg->T * cfg->d_model;
+  if (n > 0)
+    MOE_TRY_CUDA(cudaMemcpyAsync(x, x_host, n * act_bytes(*cfg), cudaMemcpyHostToDevice, s));
+  MOE_TRY(layer_forward_impl(cfg, x, w_router, router_bias, score_bias, w_gate, w_up, w_down,
+                             ws_gate, ws_up, ws_down, shared_gate, scales, y, topk_idx, topk_w,
+                             counts, drops, mean_prob, ws, ws_bytes, stream, nullptr, nullptr));
+  const size_t yb = cfg->out_dtype == MOE_BF16 ? 2 : 4;
+  if (n > 0) MOE_TRY_CUDA(cudaMemcpyAsync(y_host, y, n * yb, cudaMemcpyDeviceToHost, s));
+  return MOE_OK;
+}
+
 moe_status_t moe_layer_forward_profiled(const moe_config_t* cfg, const void* x,
                                         const void* w_router, const float* router_bias,
                                         const float* score_bias, const void* w_gate,
