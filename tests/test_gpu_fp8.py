@@ -39,7 +39,18 @@ FP8_SHAPES = {
     "multi_mtile_ntail": _shape(T=1000, d=320, E=4, k=2, F=256, F_s=128),
     "capacity": _shape(T=999, d=128, E=8, k=1, F=256, renormalize=False, capacity_factor=1.25,
                        zipf_s=1.2),
+    # shapes for the weights-in-M kernel (d_model a multiple of 256): a few
+    # rows per expert; several 64-token tiles per expert with a ragged last
+    # one and a shared expert over 5 token tiles; capacity with drops
+    "decode_shared": _shape(T=40, d=512, E=32, k=4, F=256, F_s=256, gate="sigmoid", rsf=2.5),
+    "tm_multi_tile": _shape(T=300, d=256, E=4, k=2, F=384, F_s=128),
+    "tm_capacity": _shape(T=700, d=256, E=8, k=2, F=256, capacity_factor=1.0, zipf_s=1.2),
 }
+
+# MOE_B300_FP8_LAYOUT: tokens in M (weights widened in shared memory) or
+# weights in M (widened into tensor memory); shapes the second kernel does
+# not support fall back to the first
+FP8_LAYOUTS = ["tokens_m", "weights_tm"]
 
 
 def _check_layer(s, inp, out):
@@ -53,8 +64,10 @@ def _check_layer(s, inp, out):
         assert_capacity_layer_close(np_f(out["y"]), ref["y"], ref["drop_mask"], s.name)
 
 
+@pytest.mark.parametrize("layout", FP8_LAYOUTS)
 @pytest.mark.parametrize("name", list(FP8_SHAPES))
-def test_fp8_layer_matches_oracle_all_tokens(name):
+def test_fp8_layer_matches_oracle_all_tokens(name, layout, monkeypatch):
+    monkeypatch.setenv("MOE_B300_FP8_LAYOUT", layout)
     s = FP8_SHAPES[name]
     inp = make_inputs(s, device=DEV, seed=11)
     assert inp["w_gate"].dtype == torch.float8_e4m3fn
@@ -76,9 +89,11 @@ def _every_code(shape_, gen):
     return codes.view(torch.float8_e4m3fn)
 
 
-def test_fp8_every_code_decodes_like_the_oracle():
+@pytest.mark.parametrize("layout", FP8_LAYOUTS)
+def test_fp8_every_code_decodes_like_the_oracle(layout, monkeypatch):
     # weights made of all 254 finite codes (subnormals, 448, both signs) with
     # non-power-of-two scales; the layer must match the oracle's decoding
+    monkeypatch.setenv("MOE_B300_FP8_LAYOUT", layout)
     s = _shape(T=200, d=256, E=2, k=2, F=256, gate="sigmoid", rsf=2.5)
     inp = make_inputs(s, device=DEV, seed=12)
     g = torch.Generator().manual_seed(3)
@@ -93,8 +108,13 @@ def test_fp8_every_code_decodes_like_the_oracle():
     _check_layer(s, inp, out)
 
 
+@pytest.mark.parametrize("layout", FP8_LAYOUTS)
 @pytest.mark.parametrize("F_s", [0, 256])
-def test_fp8_equals_bf16_on_decoded_weights_with_power_of_two_scales(F_s):
+def test_fp8_equals_bf16_on_decoded_weights_with_power_of_two_scales(F_s, layout, monkeypatch):
+    # the bf16 layer runs with the same MMA orientation (weights in M for the
+    # tensor-memory kernel), so the products and sums are the same
+    monkeypatch.setenv("MOE_B300_FP8_LAYOUT", layout)
+    monkeypatch.setenv("MOE_B300_EXPERT_LAYOUT", "weights_m" if layout == "weights_tm" else "tokens_m")
     s = _shape(T=515, d=256, E=8, k=2, F=256, F_s=F_s, gate="sigmoid", rsf=2.5)
     inp = make_inputs(s, device=DEV, seed=13)
     g = torch.Generator().manual_seed(4)

@@ -151,16 +151,32 @@ bool weights_in_m(const moe_config_t& c, int which) {
   return false;
 }
 
+// E4M3 GEMM layout: true = weights in M widened into tensor memory
+// (launch_gemm_fp8_tm, a weight stream for batches of a few tokens per
+// expert), false = tokens in M (launch_gemm_fp8w).  The default takes the
+// first when the average expert gets at most 64 rows and the shared expert at
+// most 256; MOE_B300_FP8_LAYOUT=tokens_m|weights_tm overrides it for tests
+// and tuning.
+bool fp8_weights_in_tmem(const moe_config_t& c) {
+  if (!fp8_tm_supported(c)) return false;
+  const char* o = getenv("MOE_B300_FP8_LAYOUT");
+  if (o && strcmp(o, "tokens_m") == 0) return false;
+  if (o && strcmp(o, "weights_tm") == 0) return true;
+  return (int64_t)c.T * c.top_k <= (int64_t)64 * c.n_experts && c.T <= 256;
+}
+
 cudaError_t run_experts(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s) {
   if (c.act_dtype != MOE_BF16) return launch_experts_simt(c, a, s);
   const bool fp8 = c.weight_format == MOE_WEIGHTS_FP8_E4M3;
+  const bool fp8_tm = fp8 && fp8_weights_in_tmem(c);
   for (int which = kGemmGateUp; which <= kGemmDown; ++which) {
     cudaEvent_t ev = which == kGemmGateUp ? a.ev_up : a.ev_down;
     if (ev) {
       const cudaError_t e = cudaEventRecord(ev, s);
       if (e != cudaSuccess) return e;
     }
-    const cudaError_t e = fp8                     ? launch_gemm_fp8w(c, a, which, s)
+    const cudaError_t e = fp8_tm                  ? launch_gemm_fp8_tm(c, a, which, s)
+                          : fp8                   ? launch_gemm_fp8w(c, a, which, s)
                           : weights_in_m(c, which) ? launch_gemm_wm(c, a, which, s)
                                                    : launch_gemm_tc(c, a, which, s);
     if (e != cudaSuccess) return e;
