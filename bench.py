@@ -477,12 +477,21 @@ def main(argv=None):
     # tensor peak (a seconds-long GEMM loop under the same cap); otherwise with
     # the burst peak.
     sustained = "sw_power_cap" in clk.get("reasons", []) and "bf16_tflops_sustained" in peaks
-    # dominant stage: the longest one
+    # dominant stage: the longest one; its bound is the roof its algorithmic
+    # work reaches first (FLOPs at the tensor peak vs bytes at the copy
+    # bandwidth): tensor for the prefill GEMMs, HBM for decode and for the
+    # Switch layer's few kept tokens over many touched experts
     dom = max(stage_ms, key=stage_ms.get)
-    if dom in ("gate_up", "down") and shape.T >= 1024:
+    tensor_key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    tensor_bound = False
+    if dom in ("gate_up", "down"):
+        f_dom = work["flops_gate_up"] if dom == "gate_up" else work["flops_down"]
+        b_dom = work["bytes_gate_up"] if dom == "gate_up" else work["bytes_down"]
+        tensor_bound = f_dom / (peaks[tensor_key] * 1e12) >= b_dom / (peaks["hbm_gbs"] * 1e9)
+    if tensor_bound:
         flops = work["flops_gate_up"] if dom == "gate_up" else work["flops_down"]
         achieved = flops / (stage_ms[dom] * 1e-3) / 1e12
-        key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+        key = tensor_key
         peak = peaks[key]
         roof = {"bound": "tensor", "kernel": f"grouped_{dom}", "achieved": achieved,
                 "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
@@ -515,6 +524,8 @@ def main(argv=None):
         "tensor_peak_frac": work["flops"] / (ms_per_step * 1e-3) / 1e12 /
                             peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"],
         "weight_gbs": work["weight_bytes"] / (ms_per_step * 1e-3) / 1e9,
+        # whole layer's weight stream against the measured copy bandwidth
+        "hbm_frac": work["weight_bytes"] / (ms_per_step * 1e-3) / 1e9 / peaks["hbm_gbs"],
         "stage_ms": stage_ms,
         "roofline": roof,
         "gpu_launches": launches,
