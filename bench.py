@@ -91,16 +91,17 @@ def load_peaks():
 
 
 # Sources of the grouped GEMM kernels whose DRAM counters profiles/traffic.json
-# stores (the bf16 tokens-in-M kernels and both E4M3 kernels).
-GEMM_SOURCES = ("experts_tc.cu", "experts_fp8.cu", "experts_fp8_tm.cu", "tc_common.cuh")
+# stores: each record names the files its kernel is built from (default: the
+# bf16 tokens-in-M kernel) and the digest of those files when it was captured.
+GEMM_SOURCES = ("experts_tc.cu", "tc_common.cuh")
 E2E_PIPELINE = 2   # batches in flight in the end-to-end leg
 
 
-def source_digest() -> str:
-    """Digest of the grouped-GEMM CUDA sources, to tell whether stored ncu
+def source_digest(names=GEMM_SOURCES) -> str:
+    """Digest of grouped-GEMM CUDA sources, to tell whether stored ncu
     counters still describe the current kernels."""
     h = hashlib.sha256()
-    files = [os.path.join(ROOT, "top_routing_expert_gate_b300", "csrc", n) for n in GEMM_SOURCES]
+    files = [os.path.join(ROOT, "top_routing_expert_gate_b300", "csrc", n) for n in names]
     for f in files:
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode())
@@ -115,7 +116,8 @@ def stored_traffic(workload: str, stage: str):
     with open(path) as f:
         t = json.load(f)
     rec = t.get(workload, {}).get(stage)
-    if not rec or rec.get("source_digest") != source_digest():
+    if not rec or rec.get("source_digest") != source_digest(tuple(rec.get("sources",
+                                                                           GEMM_SOURCES))):
         return None
     return rec.get("dram_bytes_per_launch")
 

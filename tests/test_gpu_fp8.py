@@ -48,9 +48,9 @@ FP8_SHAPES = {
 }
 
 # MOE_B300_FP8_LAYOUT: tokens in M (weights widened in shared memory) or
-# weights in M (widened into tensor memory); shapes the second kernel does
-# not support fall back to the first
-FP8_LAYOUTS = ["tokens_m", "weights_tm"]
+# weights in M (widened into tensor memory) with token tiles of 64 or 128
+# rows; shapes the second kernel does not support fall back to the first
+FP8_LAYOUTS = ["tokens_m", "weights_tm", "weights_tm128"]
 
 
 def _check_layer(s, inp, out):
@@ -114,7 +114,7 @@ def test_fp8_equals_bf16_on_decoded_weights_with_power_of_two_scales(F_s, layout
     # the bf16 layer runs with the same MMA orientation (weights in M for the
     # tensor-memory kernel), so the products and sums are the same
     monkeypatch.setenv("MOE_B300_FP8_LAYOUT", layout)
-    monkeypatch.setenv("MOE_B300_EXPERT_LAYOUT", "weights_m" if layout == "weights_tm" else "tokens_m")
+    monkeypatch.setenv("MOE_B300_EXPERT_LAYOUT", "tokens_m" if layout == "tokens_m" else "weights_m")
     s = _shape(T=515, d=256, E=8, k=2, F=256, F_s=F_s, gate="sigmoid", rsf=2.5)
     inp = make_inputs(s, device=DEV, seed=13)
     g = torch.Generator().manual_seed(4)

@@ -1,6 +1,5 @@
-// Grouped SwiGLU expert GEMMs with FP8 (E4M3) expert weights for small
-// batches (decode): the weight rows are the MMA's M and the widened weight
-// operand lives in tensor memory.
+// Grouped SwiGLU expert GEMMs with FP8 (E4M3) expert weights: the weight
+// rows are the MMA's M and the widened weight operand lives in tensor memory.
 //
 // "10. 混合专家 MoE：总参数与激活参数" (niuwancheng.cn), section
 // "推理时：显存按总参数，计算按激活参数": DeepSeek-V3 ships its weights in FP8,
@@ -12,31 +11,33 @@
 //   gate/up:  g = s_g * (X W_gate^T),  u = s_u * (X W_up^T),  h = SiLU(g) * u -> bf16
 //   down:     Y = s_d * (h W_down^T)                                          -> fp32
 //
-// A decode step gives each expert a handful of tokens, so the kernel is a
-// weight stream.  Widening the codes in shared memory (experts_fp8.cu) costs
-// a 2-byte write and a 2-byte MMA read per weight on top of the code's own
-// traffic, and shared-memory bandwidth then bounds the stream.  Here the
-// converters write the widened weights into tensor memory (tcgen05.st) and
-// tcgen05.mma reads its A operand from there; shared memory carries only the
-// codes and the small token tile.
+// Widening the codes in shared memory (experts_fp8.cu) costs a 2-byte write
+// and a 2-byte MMA read per weight on top of the code's own traffic, and
+// shared-memory bandwidth then bounds the kernel.  Here the converters write
+// the widened weights into tensor memory (tcgen05.st) and tcgen05.mma reads
+// its A operand from there; shared memory carries only the codes and the
+// token tile.  With the tokens in the MMA's N, a ragged last token tile
+// costs MMA time in proportion to its rows (N rounded up to 16).
 //
 // Tile: 256 weight rows (gate/up: 128 W_gate rows and the same 128 W_up rows;
-// down: 256 rows of W_down) x up to 64 tokens of one group, k-blocks of 128.
+// down: 256 rows of W_down) x up to TN tokens of one group (TN = 64 for small
+// batches, 128 for prefill; see TmTile), k-blocks of 128.
 //   warp 0      TMA producer of the E4M3 weight tiles (2 boxes of 128 rows x
-//               128 bytes, 128-byte swizzle) into a 5-slot ring;
+//               128 bytes, 128-byte swizzle) into a 5- or 4-slot ring;
 //   warp 1      allocates 512 TMEM columns; one thread issues, per k-block,
 //               16 tcgen05.mma (two halves x 8 K=16 steps) of M=128, N = the
 //               tile's tokens rounded up to 16, A from tensor memory, B (the
 //               tokens) from shared memory;
 //   warp 2      TMA producer of the token tiles (valid rows only, rounded up
-//               to 16) into a 3-slot ring;
-//   warps 4..7  epilogue: scales, SwiGLU, stores (thread = weight row);
+//               to 16) into a 3- or 2-slot ring;
+//   warps 4..7, 16..19  epilogue, two warps per lane quarter: scales,
+//               SwiGLU, stores (thread = weight row);
 //   warps 8..15 converters: warp (q, half) widens rows 32q..32q+31 of its
 //               half into tensor-memory lanes 32q..32q+31, 64 columns (128
 //               bf16 of K) per k-block.
 // Tensor memory: columns [0, 256) two widened-A stages of 128 columns
-// (half h at +64h); [256, 512) two accumulator buffers of 128 columns (half h
-// at +64h, one column per token).
+// (half h at +64h); [256, 512) the accumulators, 2 x TN columns per buffer
+// (half h at +TN·h, one column per token).
 #include "tc_common.cuh"
 
 namespace moe {
@@ -46,31 +47,43 @@ using namespace tc;
 
 constexpr int MBM = 128;                             // weight rows per half
 constexpr int MBK = 128;                             // K per k-block (codes per row)
-constexpr int MTN = 64;                              // tokens per tile
-constexpr int MNF = 5;                               // E4M3 slots
-constexpr int MNA = 3;                               // token slots
 constexpr int MNT = 2;                               // widened-A stages in tensor memory
 constexpr uint32_t MF_HALF = MBM * MBK;              // 16 KB: 128 rows x 128 codes
 constexpr uint32_t MF_STAGE = 2 * MF_HALF;           // 32 KB
-constexpr uint32_t MA_SUB = MTN * 128;               // 8 KB: 64 token rows x 64 bf16
-constexpr uint32_t MA_STAGE = 2 * MA_SUB;            // 16 KB: K = 128
-constexpr int kMThreads = 512;
+constexpr int kMThreads = 640;
 constexpr int kMTokWarp = 2;
-constexpr int kMEpiWarp0 = 4;
+constexpr int kMEpiWarp0 = 4;                       // and warps 16..19
 constexpr int kMConvWarp0 = 8;
 constexpr uint32_t kMTmemCols = 512;
 constexpr uint32_t kMAccCol0 = MNT * 128;            // first accumulator column
 constexpr int kMMaxGroups = kMaxExperts + 1;
 constexpr uint32_t kMCtrlBytes = 256 + 4 * (kMMaxGroups + 1 + 3 * kMMaxGroups);
-constexpr uint32_t kMSmemBytes = MNF * MF_STAGE + MNA * MA_STAGE + kMCtrlBytes + 1024;
-static_assert(kMSmemBytes <= 227 * 1024, "shared memory budget");
-static_assert(kMAccCol0 + 2 * 128 == kMTmemCols, "tensor memory budget");
+constexpr int kMMaxBoxes = 4;
+
+// Token-tile width TN and what follows from it.  TN = 64 (small batches):
+// two accumulator buffers (the epilogue of one tile overlaps the next
+// tile's MMAs), 5 E4M3 and 3 token slots.  TN = 128 (prefill): the two
+// 128-column A stages and one 256-column accumulator fill tensor memory, so
+// the accumulator is single-buffered; 4 E4M3 and 2 token slots of 32 KB.
+template <int TN>
+struct TmTile {
+  static constexpr int kTN = TN;
+  static constexpr int kNF = TN == 64 ? 5 : 4;       // E4M3 slots
+  static constexpr int kNA = TN == 64 ? 3 : 2;       // token slots
+  static constexpr int kNAcc = TN == 64 ? 2 : 1;     // accumulator buffers
+  static constexpr int kBoxes = TN == 64 ? 3 : 4;    // token boxes of TN, TN/2, .., 16 rows
+  static constexpr uint32_t kASub = TN * 128;        // TN token rows x 64 bf16
+  static constexpr uint32_t kAStage = 2 * kASub;     // K = 128
+  static constexpr uint32_t kSmem = kNF * MF_STAGE + kNA * kAStage + kMCtrlBytes + 1024;
+  static_assert(TN == 64 || TN == 128, "token tile of 64 or 128 rows");
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  static_assert(kMAccCol0 + kNAcc * 2 * TN == kMTmemCols, "tensor memory budget");
+};
 
 enum MMode { kMGateUp = 0, kMDown = 1 };
-constexpr int kMBoxes = 3;                           // token boxes of 64, 32, 16 rows
 
 struct MParams {
-  CUtensorMap a_map[2][kMBoxes];  // [kind][box]: routed grouped rows / shared-expert rows (bf16)
+  CUtensorMap a_map[2][kMMaxBoxes];  // [kind][box]: routed grouped rows / shared-expert rows (bf16)
   CUtensorMap b_map[2];     // E4M3 gate (gate/up) or down weights, box 128 B x 128 rows
   CUtensorMap u_map[2];     // E4M3 up weights (gate/up only)
   const float* b_scale[2];  // per-row scales of b_map's tensor
@@ -151,20 +164,23 @@ __device__ __forceinline__ bool warp_wait_all(uint32_t bar, uint32_t parity,
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int MODE>
+template <int MODE, int TN>
 __global__ void __launch_bounds__(kMThreads, 1)
 grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
+  using C = TmTile<TN>;
+  constexpr int MTN = C::kTN, MNF = C::kNF, MNA = C::kNA, NACC = C::kNAcc;
+  constexpr uint32_t MA_SUB = C::kASub, MA_STAGE = C::kAStage;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t sF = base;                                   // MNF x 32 KB (1024-aligned)
-  const uint32_t sA = sF + MNF * MF_STAGE;                    // MNA x 16 KB
+  const uint32_t sA = sF + MNF * MF_STAGE;                    // MNA token slots
   const uint8_t* f8 = smem;
   uint8_t* ctrl = smem + MNF * MF_STAGE + MNA * MA_STAGE;
   const uint32_t bar0 = smem_u32(ctrl);
   // barriers: wfull[MNF], wempty[MNF], afull[MNA], aempty[MNA], tfull[MNT],
-  // tempty[MNT], accf[2], acce[2], drain
+  // tempty[MNT], accf[2], acce[2] (NACC used), drain
   constexpr int kNB = 2 * MNF + 2 * MNA + 2 * MNT;
   auto wfull_bar = [&](int s) { return bar0 + 8u * s; };
   auto wempty_bar = [&](int s) { return bar0 + 8u * (MNF + s); };
@@ -216,7 +232,7 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 4);
+      mbar_init(acce_bar(b), 8);      // one arrival per epilogue warp
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -315,14 +331,14 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
         const int kind = g < p.E ? 0 : 1;
         const int nk = p.K[kind] / MBK;
         const uint32_t idesc = idesc_bf16_f32(MBM, (uint32_t)tile_n(g, m));
-        const int buf = local & 1;
-        const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
+        const int buf = local % NACC;
+        const uint32_t acc_phase = (uint32_t)(local / NACC) & 1u;
         if (!mbar_wait(acce_bar(buf), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
           failed = true;
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + kMAccCol0 + (uint32_t)(buf * 128);
+        const uint32_t d_tmem = tmem_base + kMAccCol0 + (uint32_t)(buf * 2 * MTN);
         for (int kb = 0; kb < nk; ++kb, ++i) {
           const int as = i % MNA, ts = i % MNT;
           if (!mbar_wait(afull_bar(as), (uint32_t)(i / MNA) & 1u, abort_flag, p.timeout_ns) ||
@@ -339,7 +355,8 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
                 (uint64_t)(2 * (kk & 3));
             const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
             mma_bf16_ta(d_tmem, a_tmem + (uint32_t)(8 * kk), b_desc, idesc, acc);
-            mma_bf16_ta(d_tmem + 64u, a_tmem + 64u + (uint32_t)(8 * kk), b_desc, idesc, acc);
+            mma_bf16_ta(d_tmem + (uint32_t)MTN, a_tmem + 64u + (uint32_t)(8 * kk), b_desc, idesc,
+                        acc);
           }
           mma_commit(aempty_bar(as));
           mma_commit(tempty_bar(ts));
@@ -380,8 +397,8 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
           for (int sub = 0; sub < 2; ++sub) {
             int off = 0;
 #pragma unroll
-            for (int b = 0; b < kMBoxes; ++b) {
-              const int box = 64 >> b;
+            for (int b = 0; b < C::kBoxes; ++b) {
+              const int box = MTN >> b;
               while (n_load - off >= box) {
                 tma_load_2d(sA + as * MA_STAGE + (uint32_t)sub * MA_SUB + (uint32_t)off * 128u,
                             &p.a_map[kind][b], afull_bar(as), kb * MBK + 64 * sub, a_row + off);
@@ -402,7 +419,7 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
         }
       }
     }
-  } else if (warp >= kMConvWarp0) {
+  } else if (warp >= kMConvWarp0 && warp < kMConvWarp0 + 8) {
     // ---------------- converters (warps 8..15) ----------------
     const int q = warp & 3;                    // tensor-memory lane quarter
     const int half = (warp - kMConvWarp0) >> 2;
@@ -457,16 +474,19 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
       if (lane == 0) record_error(p.status, kDevTimeout);
     }
   } else if (warp >= kMEpiWarp0) {
-    // ---------------- epilogue (warps 4..7) ----------------
+    // ---------------- epilogue (warps 4..7 and 16..19) ----------------
+    // two warps per lane quarter: part 0 (warps 4..7) and part 1 (16..19)
+    // split the tile's columns (gate/up) or its two 128-row halves (down)
     const int q = warp & 3;
+    const int part = warp >= 16 ? 1 : 0;
     const int f = q * 32 + lane;               // weight row within a half
     int local = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
       int g, m, n;
       decode(t, g, m, n);
       const int kind = g < p.E ? 0 : 1;
-      const int buf = local & 1;
-      const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
+      const int buf = local % NACC;
+      const uint32_t acc_phase = (uint32_t)(local / NACC) & 1u;
       if (!mbar_wait(accf_bar(buf), acc_phase, abort_flag, p.timeout_ns)) {
         failed = true;
         break;
@@ -475,7 +495,7 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
       const int n_valid = min(MTN, s_rows[g] - m * MTN);
       const size_t row_base = (size_t)(kind ? 0 : s_row0[g]) + (size_t)(m * MTN);
       const uint32_t tacc =
-          tmem_base + ((uint32_t)(q * 32) << 16) + kMAccCol0 + (uint32_t)(buf * 128);
+          tmem_base + ((uint32_t)(q * 32) << 16) + kMAccCol0 + (uint32_t)(buf * 2 * MTN);
       const size_t srow = (size_t)(kind ? 0 : g * p.b_rows_per_expert);
       const size_t ld = (size_t)p.ld_out[kind];
       if (MODE == kMGateUp) {
@@ -483,15 +503,16 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
         const float sg = __ldg(p.b_scale[kind] + srow + col);
         const float su = __ldg(p.u_scale[kind] + srow + col);
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out[kind]);
+        const int lo = part * (MTN / 2), hi = min(n_valid, lo + MTN / 2);
 #pragma unroll 1
-        for (int c0 = 0; c0 < n_valid; c0 += 16) {
+        for (int c0 = lo; c0 < hi; c0 += 16) {
           uint32_t gv[16], uv[16];
           tmem_ld_32x32b_x16(tacc + (uint32_t)c0, gv);
-          tmem_ld_32x32b_x16(tacc + 64u + (uint32_t)c0, uv);
+          tmem_ld_32x32b_x16(tacc + (uint32_t)(MTN + c0), uv);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            if (c0 + j < n_valid) {
+            if (c0 + j < hi) {
               const float hv = silu_f(bits_f(gv[j]) * sg) * (bits_f(uv[j]) * su);
               out[(row_base + (size_t)(c0 + j)) * ld + col] = __float2bfloat16_rn(hv);
             }
@@ -499,14 +520,14 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
         }
       } else {
         float* out = reinterpret_cast<float*>(p.out[kind]);
-#pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
+        {
+          const int hf = part;
           const size_t col = (size_t)n * 256 + (size_t)(hf * 128 + f);
           const float sd = __ldg(p.b_scale[kind] + srow + col);
 #pragma unroll 1
           for (int c0 = 0; c0 < n_valid; c0 += 16) {
             uint32_t v[16];
-            tmem_ld_32x32b_x16(tacc + (uint32_t)(hf * 64 + c0), v);
+            tmem_ld_32x32b_x16(tacc + (uint32_t)(hf * MTN + c0), v);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 16; ++j)
@@ -532,22 +553,26 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
   }
 }
 
-template <int MODE>
+template <int MODE, int TN>
 cudaError_t launch_m(const MParams& p, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(grouped_gemm_fp8_tm_kernel<MODE>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kMSmemBytes);
+    attr_err = cudaFuncSetAttribute(grouped_gemm_fp8_tm_kernel<MODE, TN>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    TmTile<TN>::kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  grouped_gemm_fp8_tm_kernel<MODE><<<num_sms(), kMThreads, kMSmemBytes, s>>>(p);
+  grouped_gemm_fp8_tm_kernel<MODE, TN><<<num_sms(), kMThreads, TmTile<TN>::kSmem, s>>>(p);
   return cudaGetLastError();
 }
 
-bool token_maps_m(CUtensorMap (&m)[kMBoxes], const void* ptr, uint64_t inner, uint64_t rows) {
+// Token boxes of tn, tn/2, .., 16 rows (64-element rows, 128-byte swizzle).
+bool token_maps_m(CUtensorMap (&m)[kMMaxBoxes], const void* ptr, uint64_t inner, uint64_t rows,
+                  int tn) {
   bool ok = true;
-  for (int b = 0; b < kMBoxes; ++b) ok &= make_map(&m[b], ptr, inner, rows, 64u >> b);
+  for (int b = 0; b < kMMaxBoxes; ++b)
+    if ((tn >> b) >= 16) ok &= make_map(&m[b], ptr, inner, rows, (uint32_t)(tn >> b));
   return ok;
 }
 
@@ -572,10 +597,10 @@ bool fp8_tm_supported(const moe_config_t& c) {
   return c.d_model % 256 == 0 && c.d_ff % 128 == 0 && shared_ok;
 }
 
-cudaError_t launch_gemm_fp8_tm(const moe_config_t& c, const ExpertArgs& a, int which,
+cudaError_t launch_gemm_fp8_tm(const moe_config_t& c, const ExpertArgs& a, int which, int tn,
                                cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
-  if (!fp8_tm_supported(c)) return cudaErrorInvalidValue;
+  if (!fp8_tm_supported(c) || (tn != 64 && tn != 128)) return cudaErrorInvalidValue;
   const int T = c.T, E = c.n_experts, d = c.d_model, F = c.d_ff, Fs = c.d_ff_shared;
   const int A = a.rows > 0 ? a.rows : T * c.top_k;
   const bool has_shared = Fs > 0 && a.ws_gate != nullptr;
@@ -590,8 +615,8 @@ cudaError_t launch_gemm_fp8_tm(const moe_config_t& c, const ExpertArgs& a, int w
   p.status = a.status;
   p.timeout_ns = kWaitTimeoutNs;
   if (which == kGemmGateUp) {
-    ok &= token_maps_m(p.a_map[0], a.x_perm, d, A);
-    ok &= token_maps_m(p.a_map[1], a.x, d, T);
+    ok &= token_maps_m(p.a_map[0], a.x_perm, d, A, tn);
+    ok &= token_maps_m(p.a_map[1], a.x, d, T, tn);
     ok &= make_map_e4m3_sw128(&p.b_map[0], a.w_gate, d, (uint64_t)E * F);
     ok &= make_map_e4m3_sw128(&p.u_map[0], a.w_up, d, (uint64_t)E * F);
     p.b_scale[0] = sc.gate_scale;
@@ -617,15 +642,15 @@ cudaError_t launch_gemm_fp8_tm(const moe_config_t& c, const ExpertArgs& a, int w
     p.N[1] = has_shared ? Fs : 128;
     p.b_rows_per_expert = F;
   } else {
-    ok &= token_maps_m(p.a_map[0], a.h, F, A);
+    ok &= token_maps_m(p.a_map[0], a.h, F, A, tn);
     ok &= make_map_e4m3_sw128(&p.b_map[0], a.w_down, F, (uint64_t)E * d);
     p.b_scale[0] = sc.down_scale;
     if (has_shared) {
-      ok &= token_maps_m(p.a_map[1], a.h_shared, Fs, T);
+      ok &= token_maps_m(p.a_map[1], a.h_shared, Fs, T, tn);
       ok &= make_map_e4m3_sw128(&p.b_map[1], a.ws_down, Fs, d);
       p.b_scale[1] = sc.shared_down_scale;
     } else {
-      for (int b = 0; b < kMBoxes; ++b) p.a_map[1][b] = p.a_map[0][b];
+      for (int b = 0; b < kMMaxBoxes; ++b) p.a_map[1][b] = p.a_map[0][b];
       p.b_map[1] = p.b_map[0];
       p.b_scale[1] = p.b_scale[0];
     }
@@ -644,7 +669,11 @@ cudaError_t launch_gemm_fp8_tm(const moe_config_t& c, const ExpertArgs& a, int w
     p.b_rows_per_expert = d;
   }
   if (!ok) return cudaErrorInvalidValue;
-  const cudaError_t err = which == kGemmGateUp ? launch_m<kMGateUp>(p, s) : launch_m<kMDown>(p, s);
+  cudaError_t err;
+  if (tn == 64)
+    err = which == kGemmGateUp ? launch_m<kMGateUp, 64>(p, s) : launch_m<kMDown, 64>(p, s);
+  else
+    err = which == kGemmGateUp ? launch_m<kMGateUp, 128>(p, s) : launch_m<kMDown, 128>(p, s);
   count_launch(a.launches);
   return err;
 }

@@ -217,10 +217,11 @@ cudaError_t launch_gemm_wm(const moe_config_t& c, const ExpertArgs& a, int which
 // Tokens in M with E4M3 expert weights widened to bf16 on chip (a.scales set).
 cudaError_t launch_gemm_fp8w(const moe_config_t& c, const ExpertArgs& a, int which,
                              cudaStream_t s);
-// E4M3 weights in M, widened into tensor memory (small batches); needs
-// fp8_tm_supported(c): d_model % 256, d_ff % 128 and d_ff_shared % 128 == 0.
+// E4M3 weights in M, widened into tensor memory, token tiles of tn = 64 or
+// 128 rows; needs fp8_tm_supported(c): d_model % 256, d_ff % 128 and
+// d_ff_shared % 128 == 0.
 bool fp8_tm_supported(const moe_config_t& c);
-cudaError_t launch_gemm_fp8_tm(const moe_config_t& c, const ExpertArgs& a, int which,
+cudaError_t launch_gemm_fp8_tm(const moe_config_t& c, const ExpertArgs& a, int which, int tn,
                                cudaStream_t s);
 
 }  // namespace moe

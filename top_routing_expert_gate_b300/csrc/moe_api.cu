@@ -151,31 +151,33 @@ bool weights_in_m(const moe_config_t& c, int which) {
   return false;
 }
 
-// E4M3 GEMM layout: true = weights in M widened into tensor memory
-// (launch_gemm_fp8_tm, a weight stream for batches of a few tokens per
-// expert), false = tokens in M (launch_gemm_fp8w).  The default takes the
-// first when the average expert gets at most 64 rows and the shared expert at
-// most 256; MOE_B300_FP8_LAYOUT=tokens_m|weights_tm overrides it for tests
-// and tuning.
-bool fp8_weights_in_tmem(const moe_config_t& c) {
-  if (!fp8_tm_supported(c)) return false;
+// E4M3 GEMM layout: the token-tile width of the weights-in-M kernel that
+// widens into tensor memory (launch_gemm_fp8_tm: 64 for batches of a few
+// tokens per expert, 128 for larger ones), or 0 for tokens in M
+// (launch_gemm_fp8w).  The default takes 64 when the average expert gets at
+// most 64 rows and the shared expert at most 256, else 128;
+// MOE_B300_FP8_LAYOUT=tokens_m|weights_tm|weights_tm128 overrides it for
+// tests and tuning.
+int fp8_tmem_tile(const moe_config_t& c) {
+  if (!fp8_tm_supported(c)) return 0;
   const char* o = getenv("MOE_B300_FP8_LAYOUT");
-  if (o && strcmp(o, "tokens_m") == 0) return false;
-  if (o && strcmp(o, "weights_tm") == 0) return true;
-  return (int64_t)c.T * c.top_k <= (int64_t)64 * c.n_experts && c.T <= 256;
+  if (o && strcmp(o, "tokens_m") == 0) return 0;
+  if (o && strcmp(o, "weights_tm") == 0) return 64;
+  if (o && strcmp(o, "weights_tm128") == 0) return 128;
+  return (int64_t)c.T * c.top_k <= (int64_t)64 * c.n_experts && c.T <= 256 ? 64 : 128;
 }
 
 cudaError_t run_experts(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s) {
   if (c.act_dtype != MOE_BF16) return launch_experts_simt(c, a, s);
   const bool fp8 = c.weight_format == MOE_WEIGHTS_FP8_E4M3;
-  const bool fp8_tm = fp8 && fp8_weights_in_tmem(c);
+  const int fp8_tn = fp8 ? fp8_tmem_tile(c) : 0;
   for (int which = kGemmGateUp; which <= kGemmDown; ++which) {
     cudaEvent_t ev = which == kGemmGateUp ? a.ev_up : a.ev_down;
     if (ev) {
       const cudaError_t e = cudaEventRecord(ev, s);
       if (e != cudaSuccess) return e;
     }
-    const cudaError_t e = fp8_tm                  ? launch_gemm_fp8_tm(c, a, which, s)
+    const cudaError_t e = fp8_tn > 0              ? launch_gemm_fp8_tm(c, a, which, fp8_tn, s)
                           : fp8                   ? launch_gemm_fp8w(c, a, which, s)
                           : weights_in_m(c, which) ? launch_gemm_wm(c, a, which, s)
                                                    : launch_gemm_tc(c, a, which, s);
