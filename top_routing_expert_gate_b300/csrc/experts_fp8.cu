@@ -14,7 +14,12 @@
 // applied once per output in the epilogue.
 //
 // Same tile layout as experts_tc.cu (tokens in the MMA's M, 128-row token
-// tiles, 256 weight rows per tile), with the weight operand widened on chip.
+// tiles, 256 weight rows per tile), with the weight operand widened on chip
+// in shared memory.  The weights-in-M kernel of experts_fp8_tm.cu, which
+// widens into tensor memory, is faster on both the decode (T = 64) and the
+// prefill (T = 8192) DeepSeek-V3-shaped layers; this one serves
+// the shapes that kernel does not take (d_model not a multiple of 256, or
+// d_ff or d_ff_shared not a multiple of 128).
 // Three rings: E4M3 weight tiles (5 slots), bf16 token tiles (3 slots) and
 // widened bf16 weight tiles (2 slots):
 //   warp 0      TMA producer of the E4M3 weight tiles (256 rows x 64 bytes,
