@@ -25,6 +25,7 @@ import statistics
 import subprocess
 import sys
 import time
+from typing import Optional
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -299,11 +300,25 @@ def tokens_per_second(tokens_per_rank: int, world: int, ms_per_step: float) -> f
     return world * tokens_per_rank / (ms_per_step * 1e-3)
 
 
-def cores_used():
+def cores_available():
     try:
         return len(os.sched_getaffinity(0))
     except AttributeError:
         return os.cpu_count() or 1
+
+
+def timed_oracle(shape, inputs, sample_tokens: int, steps: int, warmup: int = 0,
+                 threads: Optional[int] = None):
+    """Oracle timing with the BLAS pools limited to `threads` (default: every
+    core of this process's affinity); returns the step times and the BLAS
+    threads actually in effect while they ran."""
+    from threadpoolctl import threadpool_info, threadpool_limits
+    n = threads or cores_available()
+    with threadpool_limits(limits=n, user_api="blas"):
+        used = max([p["num_threads"] for p in threadpool_info() if p["user_api"] == "blas"]
+                   or [1])
+        times = time_oracle(shape, inputs, sample_tokens, steps, warmup)
+    return times, used
 
 
 # ---------------------------------------------------------------------------
@@ -335,7 +350,7 @@ def main(argv=None):
             torch.cuda.set_device(local_rank)
         dev = "cuda" if torch.cuda.is_available() else "cpu"
         inputs = make_inputs(shape, device=dev, seed=0)
-        times = time_oracle(shape, inputs, args.cpu_sample_tokens, args.steps, args.warmup)
+        times, used = timed_oracle(shape, inputs, args.cpu_sample_tokens, args.steps, args.warmup)
         t = statistics.mean(times)
         val = args.cpu_sample_tokens / t
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
@@ -343,7 +358,7 @@ def main(argv=None):
                 "ms_per_step": 1e3 * t, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": WORKLOAD_TEXT[args.workload], "name": shape.name},
-                "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores_used(),
+                "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": used,
                                  "kind": "oracle",
                                  "sample": f"per step: routing of all {shape.T} tokens + layer "
                                            f"output of {args.cpu_sample_tokens} sampled tokens"},
@@ -538,13 +553,19 @@ def main(argv=None):
                 "api": "moe_layer_forward_host", "batches_in_flight": E2E_PIPELINE},
     }
     if world == 1 and not args.no_cpu_baseline:
-        times = time_oracle(shape, inputs, args.cpu_sample_tokens, args.cpu_steps)
+        times, used = timed_oracle(shape, inputs, args.cpu_sample_tokens, args.cpu_steps)
         t = statistics.mean(times)
         line["cpu_baseline"] = {"value": args.cpu_sample_tokens / t, "unit": "tokens/s",
-                                "cores": cores_used(), "kind": "oracle",
+                                "cores": used, "kind": "oracle",
                                 "sample": f"{args.cpu_steps} oracle steps, each: routing of all "
                                           f"{T} tokens + layer output of "
                                           f"{args.cpu_sample_tokens} sampled tokens"}
+        if args.workload == "tiny":
+            # the small layer's single-thread figure beside the all-core one
+            times1, _ = timed_oracle(shape, inputs, args.cpu_sample_tokens, args.cpu_steps,
+                                     threads=1)
+            line["cpu_baseline"]["single_thread_value"] = (args.cpu_sample_tokens /
+                                                           statistics.mean(times1))
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
