@@ -214,7 +214,7 @@ moe_status_t check_shared_args(const moe_config_t* c, const void* g, const void*
 
 extern "C" {
 
-int32_t moe_version(void) { return 400; }
+int32_t moe_version(void) { return 500; }
 
 const char* moe_status_string(moe_status_t st) {
   switch (st) {
