@@ -47,6 +47,20 @@ def test_worked_example_sigmoid_scaled(golden):
     assert abs(w.sum() - 2.5) < 1e-12
 
 
+@pytest.mark.parametrize("gate,rsf,key", [("softmax", 1.0, "renormalized"),
+                                          ("sigmoid", 2.5, "scaled")])
+def test_worked_example_through_route(golden, gate, rsf, key):
+    # the full routing entry (gate dispatch, top-k, weights) on the page's example
+    g = golden("moe10_gating_worked_example.json")
+    z = np.array([g["logits"]])
+    r = O.route(z, g["k"], gate, True, rsf, None)
+    np.testing.assert_allclose(r["scores"][0], g[gate]["scores"], atol=ABS3)
+    assert r["topk_idx"][0].tolist() == g["chosen"]
+    np.testing.assert_allclose(r["topk_w"][0], g[gate][key], atol=ABS3)
+    with pytest.raises(ValueError):
+        O.gate_scores(z, "relu")
+
+
 def test_top2_softmax_renorm_closed_form():
     # renormalised top-2 softmax weight of the best expert is sigma(z1 - z2):
     # exp(z1) / (exp(z1) + exp(z2)) = 1 / (1 + exp(z2 - z1)); independent of
