@@ -311,9 +311,13 @@ def timed_oracle(shape, inputs, sample_tokens: int, steps: int, warmup: int = 0,
                  threads: Optional[int] = None):
     """Oracle timing with the BLAS pools limited to `threads` (default: every
     core of this process's affinity); returns the step times and the BLAS
-    threads actually in effect while they ran."""
-    from threadpoolctl import threadpool_info, threadpool_limits
+    threads in effect while they ran.  Without threadpoolctl the BLAS
+    default (one thread per core) stays and the affinity count is reported."""
     n = threads or cores_available()
+    try:
+        from threadpoolctl import threadpool_info, threadpool_limits
+    except ImportError:
+        return time_oracle(shape, inputs, sample_tokens, steps, warmup), n
     with threadpool_limits(limits=n, user_api="blas"):
         used = max([p["num_threads"] for p in threadpool_info() if p["user_api"] == "blas"]
                    or [1])
