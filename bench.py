@@ -295,6 +295,16 @@ def max_over_ranks(value: float, device) -> float:
     return float(t.item())
 
 
+def tensor_bound(work, stage: str, peaks, tensor_key: str) -> bool:
+    """True when a GEMM stage's algorithmic FLOPs take longer at the tensor
+    peak than its algorithmic weight bytes at the copy bandwidth."""
+    if stage not in ("gate_up", "down"):
+        return False
+    f = work["flops_gate_up"] if stage == "gate_up" else work["flops_down"]
+    b = work["bytes_gate_up"] if stage == "gate_up" else work["bytes_down"]
+    return f / (peaks[tensor_key] * 1e12) >= b / (peaks["hbm_gbs"] * 1e9)
+
+
 def tokens_per_second(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
     """Whole-job throughput: every rank's tokens over the slowest rank's time."""
     return world * tokens_per_rank / (ms_per_step * 1e-3)
@@ -504,12 +514,7 @@ def main(argv=None):
     # Switch layer's few kept tokens over many touched experts
     dom = max(stage_ms, key=stage_ms.get)
     tensor_key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
-    tensor_bound = False
-    if dom in ("gate_up", "down"):
-        f_dom = work["flops_gate_up"] if dom == "gate_up" else work["flops_down"]
-        b_dom = work["bytes_gate_up"] if dom == "gate_up" else work["bytes_down"]
-        tensor_bound = f_dom / (peaks[tensor_key] * 1e12) >= b_dom / (peaks["hbm_gbs"] * 1e9)
-    if tensor_bound:
+    if tensor_bound(work, dom, peaks, tensor_key):
         flops = work["flops_gate_up"] if dom == "gate_up" else work["flops_down"]
         achieved = flops / (stage_ms[dom] * 1e-3) / 1e12
         key = tensor_key
