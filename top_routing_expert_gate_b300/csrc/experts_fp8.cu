@@ -36,7 +36,7 @@
 // positions (exponent bias 7 kept), then one bf16x2 multiply by 2^120 rebiases
 // to 127; subnormal codes come out exact because the multiply sees them as
 // bf16 subnormals.  NaN codes (S.1111.111) are out of contract.
-#include "tc_common.cuh"
+#include "fp8_common.cuh"
 
 namespace moe {
 namespace {
@@ -95,28 +95,6 @@ __device__ __forceinline__ int q_n_tiles(int mode, int N) {
 // (tensor core operand reads, TMA) once this fence is followed by a barrier.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Two E4M3 codes placed in the high bytes of two 16-bit halves ([0, b0, 0, b1])
-// -> the two values as bf16x2.
-__device__ __forceinline__ uint32_t e4m3x2_hi_to_bf16x2(uint32_t t) {
-  const uint32_t bits = (t & 0x80008000u) | ((t >> 4) & 0x07F007F0u);
-  uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(bits), "r"(0x7B807B80u));   // x 2^120
-  return r;
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(a), "r"(sel));
-  return r;
-}
-
-// Waits in every lane; the warp agrees on the outcome.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
-                                          uint64_t timeout_ns) {
-  const bool ok = mbar_wait(bar, parity, abort, timeout_ns);
-  return __all_sync(0xffffffffu, ok);
 }
 
 template <int MODE>
@@ -389,10 +367,8 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ QParams p) {
           const int q = ct + kConvThreads * j;
           const int r = q >> 3, c = q & 7;
           uint4 o;
-          o.x = e4m3x2_hi_to_bf16x2(prmt(v[j].x, 0x1404u));
-          o.y = e4m3x2_hi_to_bf16x2(prmt(v[j].x, 0x3424u));
-          o.z = e4m3x2_hi_to_bf16x2(prmt(v[j].y, 0x1404u));
-          o.w = e4m3x2_hi_to_bf16x2(prmt(v[j].y, 0x3424u));
+          e4m3x4_to_bf16x4(v[j].x, o.x, o.y);
+          e4m3x4_to_bf16x4(v[j].y, o.z, o.w);
           *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = o;
         }
         fence_proxy_async_smem();

@@ -38,7 +38,7 @@
 // Tensor memory: columns [0, 256) two widened-A stages of 128 columns
 // (half h at +64h); [256, 512) the accumulators, 2 x TN columns per buffer
 // (half h at +TN·h, one column per token).
-#include "tc_common.cuh"
+#include "fp8_common.cuh"
 
 namespace moe {
 namespace {
@@ -133,35 +133,6 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
 }
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// Two E4M3 codes placed in the high bytes of two 16-bit halves ([0, b0, 0, b1])
-// -> the two values as bf16x2: sign, exponent and mantissa moved into bf16
-// positions with the bias-7 exponent kept, then x 2^120 rebiases to 127
-// (subnormal codes are bf16 subnormals before the multiply and come out exact).
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t t) {
-  const uint32_t bits = (t & 0x80008000u) | ((t >> 4) & 0x07F007F0u);
-  uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(bits), "r"(0x7B807B80u));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t prmt0(uint32_t a, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(a), "r"(sel));
-  return r;
-}
-
-// Four codes (one 32-bit word, code j in byte j) -> bf16 of codes 0,1 and 2,3.
-__device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  lo = e4m3x2_to_bf16x2(prmt0(w, 0x1404u));
-  hi = e4m3x2_to_bf16x2(prmt0(w, 0x3424u));
-}
-
-__device__ __forceinline__ bool warp_wait_all(uint32_t bar, uint32_t parity,
-                                              const volatile int* abort, uint64_t timeout_ns) {
-  const bool ok = mbar_wait(bar, parity, abort, timeout_ns);
-  return __all_sync(0xffffffffu, ok);
 }
 
 template <int MODE, int TN>
@@ -433,9 +404,9 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
       const int nk = p.K[kind] / MBK;
       for (int kb = 0; kb < nk; ++kb, ++i) {
         const int fs = i % MNF, ts = i % MNT;
-        if (!warp_wait_all(tempty_bar(ts), ((uint32_t)(i / MNT) & 1u) ^ 1u, abort_flag,
+        if (!warp_wait(tempty_bar(ts), ((uint32_t)(i / MNT) & 1u) ^ 1u, abort_flag,
                            p.timeout_ns) ||
-            !warp_wait_all(wfull_bar(fs), (uint32_t)(i / MNF) & 1u, abort_flag, p.timeout_ns)) {
+            !warp_wait(wfull_bar(fs), (uint32_t)(i / MNF) & 1u, abort_flag, p.timeout_ns)) {
           failed = true;
           break;
         }
@@ -453,10 +424,10 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const uint4 w = v[4 * h2 + c];
-            widen4(w.x, o[8 * c + 0], o[8 * c + 1]);
-            widen4(w.y, o[8 * c + 2], o[8 * c + 3]);
-            widen4(w.z, o[8 * c + 4], o[8 * c + 5]);
-            widen4(w.w, o[8 * c + 6], o[8 * c + 7]);
+            e4m3x4_to_bf16x4(w.x, o[8 * c + 0], o[8 * c + 1]);
+            e4m3x4_to_bf16x4(w.y, o[8 * c + 2], o[8 * c + 3]);
+            e4m3x4_to_bf16x4(w.z, o[8 * c + 4], o[8 * c + 5]);
+            e4m3x4_to_bf16x4(w.w, o[8 * c + 6], o[8 * c + 7]);
           }
           tmem_st_32x32b_x32(t_row + (uint32_t)(ts * 128 + 32 * h2), o);
         }
