@@ -243,16 +243,19 @@ MOE_API moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* topk_i
  *     into the library, held on every GPU that loads it until the process
  *     exits.  Limit: T * top_k <= 131072 assignments (and n_experts <= 256);
  *     larger batches return MOE_ERR_UNSUPPORTED without launching anything.
- *   - The first call on each device looks up that array's device address
- *     (cudaGetSymbolAddress) with that device current; make this first call
- *     before any stream capture.
+ *   - Every call looks up that array's device address on the current
+ *     device (cudaGetSymbolAddress, a host-side lookup), so the address stays
+ *     right after cudaDeviceReset.  The first call on a device may also load
+ *     the library's device code there; make that first call before any
+ *     stream capture.
  *   - All calls in the process share the one array: calls whose GPU work may
  *     overlap (different streams, or different host threads on one device)
  *     race on it and must be serialised by the caller.
  *   - There is no status word: an expert index outside [0, E) is not counted
  *     anywhere and its assignment is marked dropped, so sum(counts) +
  *     sum(drops) < T * top_k reveals it.
- * Arguments, outputs and determinism are those of moe_dispatch. */
+ * Arguments, configuration rules (token-choice routing only), outputs and
+ * determinism are those of moe_dispatch. */
 MOE_API moe_status_t moe_dispatch_no_workspace(const moe_config_t* cfg, const int32_t* topk_idx,
                                                int32_t* counts, int32_t* drops,
                                                int32_t* offsets, int32_t* perm,

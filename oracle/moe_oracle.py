@@ -15,7 +15,7 @@ method, step by step, with no blocking, fusion or reordering:
 Layout conventions (nn.Linear orientation, out x in): x [T,d], w_router [E,d],
 expert e: w_gate [F,d], w_up [F,d], w_down [d,F]; shared expert likewise.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * top-k ties go to the lower expert index; the chosen list is ordered by
     logit descending, then index ascending;
   * the selection key is the raw logit z (softmax and sigmoid are strictly

@@ -8,6 +8,7 @@ from typing import Optional, Sequence
 import numpy as np
 import torch
 
+import top_routing_expert_gate_b300 as moe
 from oracle import moe_oracle as O
 from workloads.generate import ExpertWeights, shared_weights, to_f64
 
@@ -120,8 +121,13 @@ def layer_shared(inputs):
     return shared_weights(inputs)
 
 
-def oracle_layer(shape, inputs, tokens: Optional[Sequence[int]] = None):
-    """Run the float64 oracle on the (bf16/fp32/E4M3) inputs, widened exactly."""
+def oracle_layer(shape, inputs, tokens: Optional[Sequence[int]] = None,
+                 logits: Optional[np.ndarray] = None):
+    """Run the float64 oracle on the (bf16/fp32/E4M3) inputs, widened exactly.
+
+    ``logits`` (the library's fp32 router logits, router bias included)
+    replace the oracle's own x . W^T: routing is then decided on the same
+    numbers on both sides, so its outputs must agree bit for bit."""
     T = inputs["x"].shape[0]
     return O.moe_layer_forward(
         to_f64(inputs["x"]), to_f64(inputs["w_router"]),
@@ -129,9 +135,75 @@ def oracle_layer(shape, inputs, tokens: Optional[Sequence[int]] = None):
         k=shape.k, gate=shape.gate, renormalize=shape.renormalize,
         routed_scaling_factor=shape.rsf, capacity=oracle_capacity(shape, T),
         router_bias=to_f64(inputs["router_bias"]), shared=layer_shared(inputs),
-        tokens=tokens, score_bias=to_f64(inputs.get("score_bias")),
+        tokens=tokens, logits=logits, score_bias=to_f64(inputs.get("score_bias")),
         n_group=max(shape.n_group, 1), topk_group=shape.topk_group,
         shared_gate=to_f64(inputs.get("shared_gate")))
+
+
+def oracle_route(shape, logits: np.ndarray):
+    """The oracle's routing and dispatch of the whole batch from given logits."""
+    T = logits.shape[0]
+    return O.route(logits, shape.k, shape.gate, shape.renormalize, shape.rsf,
+                   oracle_capacity(shape, T))
+
+
+def library_routing(cfg, inputs, ws):
+    """The library's routing of the whole batch through the split entry
+    points: fp32 logits (x . W^T plus the router bias, the numbers the layer
+    ranks), top-k indices and weights, mean probability, and the dispatch
+    arrays.  Enqueued on the current stream; synchronise before reading."""
+    w = moe.LayerWeights.from_inputs(inputs)
+    r = moe.route(cfg, inputs["x"], w.w_router, w.router_bias, ws=ws, score_bias=w.score_bias)
+    r.update(moe.dispatch(cfg, r["topk_idx"], ws=ws))
+    return r
+
+
+# Router weights from the same fp32 logits: fp32 exp and division against
+# float64, a few ulp apart.
+WEIGHT_REL_SHARED = 2e-6
+
+
+def assert_routing_bit_exact(lib, ref, T: int, k: int):
+    """Check (a): fed the same fp32 logits, top-k indices, counts, drops,
+    offsets, permutation and drop mask agree bit for bit; the weights within
+    a few ulp."""
+    A = T * k
+    np.testing.assert_array_equal(np_i(lib["topk_idx"]), ref["topk_idx"])
+    np.testing.assert_array_equal(np_i(lib["counts"]), ref["counts"])
+    np.testing.assert_array_equal(np_i(lib["drops"]), ref["drops"])
+    np.testing.assert_array_equal(np_i(lib["offsets"]), ref["offsets"])
+    n = int(ref["offsets"][-1])
+    np.testing.assert_array_equal(np_i(lib["perm"])[:n], ref["perm"][:n])
+    np.testing.assert_array_equal(np_i(lib["drop_mask"])[:A], ref["drop_mask"])
+    np.testing.assert_allclose(np_f(lib["topk_w"]), ref["topk_w"], rtol=WEIGHT_REL_SHARED,
+                               atol=2e-7)
+
+
+def ragged_tail_tokens(ref, k: int) -> np.ndarray:
+    """For every expert that kept a row, the token of its last grouped row:
+    that row lies in the expert's last (ragged) row tile, next to the first
+    row of the following expert, in every tile layout."""
+    offs, perm = ref["offsets"], ref["perm"]
+    toks = [int(perm[offs[e + 1] - 1]) // k for e in range(len(offs) - 1) if offs[e + 1] > offs[e]]
+    return np.unique(np.asarray(toks, dtype=np.int64))
+
+
+def check_tokens(ref, T: int, k: int, n: int, seed: int = 0) -> np.ndarray:
+    """Tokens whose outputs a sampled comparison checks: each expert's
+    ragged-tail token, the first and last token (the shared expert's first
+    and last row tile), up to 8 tokens with a dropped choice and up to 8
+    whose every choice was dropped, then random tokens up to ``n`` in all."""
+    rng = np.random.default_rng(seed)
+    pick = set(ragged_tail_tokens(ref, k).tolist()) | {0, T - 1}
+    drop = np.asarray(ref["drop_mask"]).reshape(T, k) != 0
+    for mask in (drop.any(axis=1) & ~drop.all(axis=1), drop.all(axis=1)):
+        cand = np.flatnonzero(mask)
+        if len(cand):
+            pick |= set(rng.choice(cand, min(8, len(cand)), replace=False).tolist())
+    rest = np.setdiff1d(np.arange(T), np.fromiter(pick, dtype=np.int64))
+    if len(pick) < n and len(rest):
+        pick |= set(rng.choice(rest, min(n - len(pick), len(rest)), replace=False).tolist())
+    return np.sort(np.fromiter(pick, dtype=np.int64))
 
 
 def biased_margins(scores: np.ndarray, bias: Optional[np.ndarray], idx: np.ndarray,

@@ -241,3 +241,30 @@ def test_config_from_shape_capacity():
     assert c.capacity == 320 and c.top_k == 1 and c.renormalize == 0
     c = moe.config_from_shape(SHAPES["dsv3_prefill"])
     assert c.capacity == -1 and abs(c.routed_scaling_factor - 2.5) < 1e-7 and c.gate == 1
+
+
+def test_no_workspace_dispatch_applies_the_dispatch_config_rules():
+    # moe_dispatch_no_workspace validates the configuration as moe_dispatch
+    # does (and refuses expert-choice routing) before any CUDA call
+    lib = B.load_library()
+    fake = 0x10000   # never dereferenced: validation fails first
+
+    def call(c):
+        return lib.moe_dispatch_no_workspace(ctypes.byref(c), fake, fake, fake, fake, fake, fake,
+                                             None)
+
+    assert call(_cfg(routing="expert")) == B.MOE_ERR_INVALID_ARG
+    c = _cfg()
+    c.gate = 7
+    assert call(c) == B.MOE_ERR_INVALID_ARG
+    c = _cfg()
+    c.d_ff = 0
+    assert call(c) == B.MOE_ERR_INVALID_ARG
+    c = _cfg()
+    c.top_k = c.n_experts + 1
+    assert call(c) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch_no_workspace(None, fake, fake, fake, fake, fake, fake,
+                                         None) == B.MOE_ERR_INVALID_ARG
+    # misaligned output pointer
+    assert lib.moe_dispatch_no_workspace(ctypes.byref(_cfg()), fake, fake + 4, fake, fake, fake,
+                                         fake, None) == B.MOE_ERR_INVALID_ARG

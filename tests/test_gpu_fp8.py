@@ -17,8 +17,11 @@ import top_routing_expert_gate_b300 as moe
 from oracle import moe_oracle as O
 from workloads import SHAPES, MoEShape, make_inputs
 
-from gpu_util import (MARGIN, assert_capacity_layer_close, assert_layer_close, np_f, np_i,
-                      oracle_layer, same_sets, score_margins)
+from workloads.generate import to_f64
+
+from gpu_util import (MARGIN, assert_capacity_layer_close, assert_layer_close,
+                      assert_routing_bit_exact, check_tokens, library_routing, np_f, np_i,
+                      oracle_layer, oracle_route, same_sets, score_margins)
 
 pytestmark = pytest.mark.gpu
 
@@ -53,15 +56,26 @@ FP8_SHAPES = {
 FP8_LAYOUTS = ["tokens_m", "weights_tm", "weights_tm128"]
 
 
-def _check_layer(s, inp, out):
-    ref = oracle_layer(s, inp)
-    same = same_sets(np_i(out["topk_idx"]), ref["topk_idx"])
-    margins = score_margins(ref["scores"], ref["topk_idx"])
-    assert np.all(same[margins > MARGIN])
+def _check_layer(s, inp, cfg, ws, out):
+    """The layer against the oracle routed from the library's fp32 logits:
+    routing and dispatch bit for bit, the output on every token (capacity
+    layers included); then the end-to-end routing rule on margin-clear
+    tokens."""
+    lib = library_routing(cfg, inp, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_error(ws) == 0
+    assert torch.equal(lib["topk_idx"], out["topk_idx"])
+    ref = oracle_layer(s, inp, logits=np_f(lib["logits"]))
+    assert_routing_bit_exact(lib, ref, s.T, s.k)
     if s.capacity_factor is None:
-        assert_layer_close(np_f(out["y"])[same], ref["y"][same], s.name)
-    elif same.all():
+        assert_layer_close(np_f(out["y"]), ref["y"], s.name)
+    else:
+        assert ref["drops"].sum() > 0
         assert_capacity_layer_close(np_f(out["y"]), ref["y"], ref["drop_mask"], s.name)
+    ref_b = oracle_route(s, O.router_logits(to_f64(inp["x"]), to_f64(inp["w_router"]),
+                                            to_f64(inp["router_bias"])))
+    same = same_sets(np_i(out["topk_idx"]), ref_b["topk_idx"])
+    assert np.all(same[score_margins(ref_b["scores"], ref_b["topk_idx"]) > MARGIN])
 
 
 @pytest.mark.parametrize("layout", FP8_LAYOUTS)
@@ -74,9 +88,7 @@ def test_fp8_layer_matches_oracle_all_tokens(name, layout, monkeypatch):
     cfg = moe.config_from_shape(s)
     ws = moe.Workspace(cfg)
     out = moe.layer_forward(cfg, inp["x"], moe.LayerWeights.from_inputs(inp), ws=ws)
-    torch.cuda.synchronize()
-    assert moe.moe_get_error(ws) == 0
-    _check_layer(s, inp, out)
+    _check_layer(s, inp, cfg, ws, out)
 
 
 def _every_code(shape_, gen):
@@ -103,9 +115,9 @@ def test_fp8_every_code_decodes_like_the_oracle(layout, monkeypatch):
         inp[key + "_scale"] = (torch.rand(rows[:2], generator=g) * 0.5 + 0.5).mul(
             1.0 / (200.0 * np.sqrt(fan_in))).to(DEV)
     cfg = moe.config_from_shape(s)
-    out = moe.layer_forward(cfg, inp["x"], moe.LayerWeights.from_inputs(inp))
-    torch.cuda.synchronize()
-    _check_layer(s, inp, out)
+    ws = moe.Workspace(cfg)
+    out = moe.layer_forward(cfg, inp["x"], moe.LayerWeights.from_inputs(inp), ws=ws)
+    _check_layer(s, inp, cfg, ws, out)
 
 
 @pytest.mark.parametrize("layout", FP8_LAYOUTS)
@@ -138,22 +150,26 @@ def test_fp8_equals_bf16_on_decoded_weights_with_power_of_two_scales(F_s, layout
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["dsv3_decode_fp8", "dsv3_prefill_fp8"])
-def test_full_size_fp8_layer_sampled(name):
+@pytest.mark.parametrize("name,n_check", [("dsv3_decode_fp8", 64), ("dsv3_prefill_fp8", 320)])
+def test_full_size_fp8_layer_sampled(name, n_check):
+    # the benchmark's launch configuration; the decode batch is compared on
+    # all 64 tokens, prefill on every expert's ragged-tail token plus random ones
     s = SHAPES[name]
     inp = make_inputs(s, device=DEV, seed=0)
     cfg = moe.config_from_shape(s)
     ws = moe.Workspace(cfg)
     out = moe.layer_forward(cfg, inp["x"], moe.LayerWeights.from_inputs(inp), ws=ws)
+    lib = library_routing(cfg, inp, ws)
     torch.cuda.synchronize()
     assert moe.moe_get_error(ws) == 0
-    from workloads.generate import to_f64
+    assert torch.equal(lib["topk_idx"], out["topk_idx"])
+    ref = oracle_route(s, np_f(lib["logits"]))
+    assert_routing_bit_exact(lib, ref, s.T, s.k)
     z = O.router_logits(to_f64(inp["x"]), to_f64(inp["w_router"]))
-    ref = O.route(z, s.k, s.gate, s.renormalize, s.rsf, None)
-    gi = np_i(out["topk_idx"])
-    same = same_sets(gi, ref["topk_idx"])
-    assert np.all(same[score_margins(ref["scores"], ref["topk_idx"]) > MARGIN])
-    rng = np.random.default_rng(0)
-    pick = np.sort(rng.choice(np.arange(s.T)[same], min(24, int(same.sum())), replace=False))
-    oref = oracle_layer(s, inp, tokens=pick)
+    ref_b = oracle_route(s, z)
+    same = same_sets(np_i(out["topk_idx"]), ref_b["topk_idx"])
+    assert np.all(same[score_margins(ref_b["scores"], ref_b["topk_idx"]) > MARGIN])
+    pick = check_tokens(ref, s.T, s.k, n_check)
+    assert len(pick) >= min(n_check, s.T)
+    oref = oracle_layer(s, inp, tokens=pick, logits=np_f(lib["logits"]))
     assert_layer_close(np_f(out["y"])[pick], oref["y"], name)

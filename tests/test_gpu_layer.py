@@ -16,8 +16,10 @@ from oracle import moe_oracle as O
 from workloads import SHAPES, MoEShape, make_inputs
 from workloads.generate import to_f64
 
-from gpu_util import (MARGIN, assert_capacity_layer_close, assert_layer_close, np_f, np_i,
-                      oracle_layer, same_sets, score_margins)
+from gpu_util import (MARGIN, WEIGHT_REL_SHARED, assert_capacity_layer_close,
+                      assert_layer_close, assert_routing_bit_exact, check_tokens,
+                      library_routing, np_f, np_i, oracle_layer, oracle_route, same_sets,
+                      score_margins)
 
 pytestmark = pytest.mark.gpu
 
@@ -45,6 +47,10 @@ MID_SHAPES = {
                                  rsf=2.5),
     "mid_capacity_zipf": _shape(T=999, d=128, E=8, k=1, F=256, renormalize=False,
                                 capacity_factor=1.25, zipf_s=1.2),
+    # top-2 with a capacity: second choices compete for slots with later
+    # tokens' first choices; several row tiles per expert, a shared expert
+    "mid_capacity_k2": _shape(T=1200, d=256, E=8, k=2, F=256, F_s=128, capacity_factor=2.0,
+                              zipf_s=1.2),
     "mid_many_experts": _shape(T=129, d=128, E=64, k=6, F=128, F_s=128, gate="sigmoid",
                                rsf=2.5),
     "mid_fp32_shared": _shape(T=77, d=64, E=5, k=3, F=96, F_s=32, dtype="fp32"),
@@ -61,30 +67,63 @@ MID_SHAPES = {
 }
 
 
+def _layer_and_routing(s, inp, ws=None):
+    """The fused layer call and, on the same workspace, the split routing
+    entry points that expose the fp32 logits and the dispatch arrays."""
+    cfg = moe.config_from_shape(s, T=inp["x"].shape[0])
+    ws = ws or moe.Workspace(cfg)
+    out = moe.layer_forward(cfg, inp["x"], moe.LayerWeights.from_inputs(inp), ws=ws)
+    lib = library_routing(cfg, inp, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_error(ws) == 0
+    assert torch.equal(lib["topk_idx"], out["topk_idx"])
+    return cfg, out, lib
+
+
 @pytest.mark.parametrize("layout", ["tokens_m", "weights_m"])
 @pytest.mark.parametrize("name", list(MID_SHAPES))
 def test_layer_matches_oracle_all_tokens(name, layout, monkeypatch):
-    # both tile layouts of the bf16 grouped GEMMs (tokens or weights in the MMA's M)
+    # both tile layouts of the bf16 grouped GEMMs (tokens or weights in the
+    # MMA's M).  The oracle routes from the library's fp32 logits, so (a) the
+    # routing and dispatch arrays must agree bit for bit and (c) the output is
+    # compared on every token, capacity layers included.
     monkeypatch.setenv("MOE_B300_EXPERT_LAYOUT", layout)
     s = MID_SHAPES[name]
     inp = make_inputs(s, device=DEV, seed=1)
-    cfg, out = _run_layer(s, inp)
+    cfg, out, lib = _layer_and_routing(s, inp)
+    ref = oracle_layer(s, inp, logits=np_f(lib["logits"]))
+    assert_routing_bit_exact(lib, ref, s.T, s.k)
+    np.testing.assert_array_equal(np_i(out["counts"]), ref["counts"])
+    np.testing.assert_array_equal(np_i(out["drops"]), ref["drops"])
+    np.testing.assert_allclose(np_f(out["topk_w"]), ref["topk_w"], rtol=WEIGHT_REL_SHARED,
+                               atol=2e-7)
+    if s.capacity_factor is None:
+        assert_layer_close(np_f(out["y"]), ref["y"], name)
+    else:
+        assert ref["drops"].sum() > 0, "the capacity shape must drop assignments"
+        assert_capacity_layer_close(np_f(out["y"]), ref["y"], ref["drop_mask"], name)
+    np.testing.assert_allclose(np_f(out["mean_prob"]), ref["mean_prob"], atol=1e-4)
+
+
+@pytest.mark.parametrize("name", list(MID_SHAPES))
+def test_layer_end_to_end_routing(name):
+    # (b) the oracle computes its own float64 logits: every token whose
+    # k-th/(k+1)-th score margin exceeds 1e-3 chooses the same experts, and
+    # (without a capacity, where one flipped token cannot move other tokens'
+    # slots) the output of every token with the same chosen set is within
+    # the layer tolerance
+    s = MID_SHAPES[name]
+    inp = make_inputs(s, device=DEV, seed=1)
+    cfg, out, lib = _layer_and_routing(s, inp)
     ref = oracle_layer(s, inp)
     margins = score_margins(ref["scores"], ref["topk_idx"])
     same = same_sets(np_i(out["topk_idx"]), ref["topk_idx"])
     assert np.all(same[margins > MARGIN])
+    assert same.mean() > 0.9
+    np.testing.assert_array_equal(np_i(out["counts"]) + np_i(out["drops"]),
+                                  np.bincount(np_i(out["topk_idx"]).ravel(), minlength=s.E))
     if s.capacity_factor is None:
         assert_layer_close(np_f(out["y"])[same], ref["y"][same], name)
-    else:
-        # a flipped ambiguous token can move later slots of its experts
-        if same.all():
-            np.testing.assert_array_equal(np_i(out["counts"]), ref["counts"])
-            np.testing.assert_array_equal(np_i(out["drops"]), ref["drops"])
-            assert_capacity_layer_close(np_f(out["y"]), ref["y"], ref["drop_mask"], name)
-    # statistics
-    if same.all():
-        np.testing.assert_array_equal(np_i(out["counts"]) + np_i(out["drops"]),
-                                      np.bincount(ref["topk_idx"].ravel(), minlength=s.E))
     np.testing.assert_allclose(np_f(out["mean_prob"]), ref["mean_prob"], atol=1e-4)
 
 
@@ -264,10 +303,13 @@ def test_balance_loss_from_layer_statistics():
 
 
 # ---------------------------------------------------------------------------
-# The five full-size layers, sampled tokens
+# The five full-size layers, in the benchmark's launch configuration
 # ---------------------------------------------------------------------------
 
 FULL = ["tiny", "mixtral", "dsv3_prefill", "switch", "dsv3_decode"]
+# tokens whose outputs the oracle computes at full size (all of them for the
+# small batches); each expert's ragged last row tile is always among them
+FULL_CHECK = {"tiny": 64, "mixtral": 64, "dsv3_prefill": 320, "switch": 96, "dsv3_decode": 64}
 
 
 @pytest.mark.slow
@@ -275,47 +317,28 @@ FULL = ["tiny", "mixtral", "dsv3_prefill", "switch", "dsv3_decode"]
 def test_full_size_layer_sampled(name):
     s = SHAPES[name]
     inp = make_inputs(s, device=DEV, seed=0)
-    cfg = moe.config_from_shape(s)
-    ws = moe.Workspace(cfg)
-    w = moe.LayerWeights.from_inputs(inp)
-    out = moe.layer_forward(cfg, inp["x"], w, ws=ws)
-    # routing through the split path gives the drop mask
-    r = moe.route(cfg, inp["x"], w.w_router, w.router_bias, ws=ws)
-    dsp = moe.dispatch(cfg, r["topk_idx"], ws=ws)
-    torch.cuda.synchronize()
-    assert moe.moe_get_error(ws) == 0
-    assert torch.equal(r["topk_idx"], out["topk_idx"])
-    rng = np.random.default_rng(0)
-    n_sample = min(s.T, 24)
-    cand = np.arange(s.T)
-    # routing reference for every token (capacity needs all of them)
-    z = O.router_logits(to_f64(inp["x"]), to_f64(inp["w_router"]), to_f64(inp["router_bias"]))
-    C = O.expert_capacity(s.T, s.E, s.capacity_factor)
-    ref = O.route(z, s.k, s.gate, s.renormalize, s.rsf, C)
-    gi = np_i(out["topk_idx"])
-    gdrop = np_i(dsp["drop_mask"])[: s.T * s.k].reshape(s.T, s.k)
-    # same chosen set, and (with a capacity) the same kept/dropped choices
-    same = same_sets(gi, ref["topk_idx"])
-    if C is not None:
-        same &= np.all(gi == ref["topk_idx"], axis=1) & \
-            np.all(gdrop == ref["drop_mask"].reshape(s.T, s.k), axis=1)
-    margins = score_margins(ref["scores"], ref["topk_idx"])
-    if C is None:
-        assert np.all(same[margins > MARGIN])
-    assert same.mean() > 0.97
+    cfg, out, lib = _layer_and_routing(s, inp)
+    # (a) from the library's fp32 logits: routing and dispatch bit for bit
+    ref = oracle_route(s, np_f(lib["logits"]))
+    assert_routing_bit_exact(lib, ref, s.T, s.k)
+    np.testing.assert_array_equal(np_i(out["counts"]), ref["counts"])
+    np.testing.assert_array_equal(np_i(out["drops"]), ref["drops"])
     np.testing.assert_allclose(np_f(out["mean_prob"]), ref["mean_prob"], atol=1e-4)
-    if same.all():
-        np.testing.assert_array_equal(np_i(out["counts"]), ref["counts"])
-        np.testing.assert_array_equal(np_i(out["drops"]), ref["drops"])
-    # sampled outputs: tokens with identical routing, including dropped ones
-    pool = cand[same]
-    if C is not None:
-        dropped_any = pool[ref["drop_mask"].reshape(s.T, s.k)[pool].any(axis=1)]
-        kept = pool[~ref["drop_mask"].reshape(s.T, s.k)[pool].any(axis=1)]
-        pick = np.concatenate([rng.choice(dropped_any, min(4, len(dropped_any)), replace=False),
-                               rng.choice(kept, min(n_sample - 4, len(kept)), replace=False)])
+    # (b) end to end: margin-clear tokens choose the same experts
+    z = O.router_logits(to_f64(inp["x"]), to_f64(inp["w_router"]), to_f64(inp["router_bias"]))
+    ref_b = oracle_route(s, z)
+    same = same_sets(np_i(out["topk_idx"]), ref_b["topk_idx"])
+    assert np.all(same[score_margins(ref_b["scores"], ref_b["topk_idx"]) > MARGIN])
+    assert same.mean() > 0.97
+    # (c) outputs: every expert's ragged-tail token, the shared expert's first
+    # and last tiles, dropped tokens, random ones
+    pick = check_tokens(ref, s.T, s.k, FULL_CHECK[name])
+    assert len(pick) >= min(FULL_CHECK[name], s.T)
+    oref = oracle_layer(s, inp, tokens=pick, logits=np_f(lib["logits"]))
+    y = np_f(out["y"])[pick]
+    if s.capacity_factor is None:
+        assert_layer_close(y, oref["y"], name)
     else:
-        pick = rng.choice(pool, min(n_sample, len(pool)), replace=False)
-    pick = np.sort(pick)
-    oref = oracle_layer(s, inp, tokens=pick)
-    assert_layer_close(np_f(out["y"])[pick], oref["y"], name)
+        dm = ref["drop_mask"].reshape(s.T, s.k)[pick]
+        assert dm.any() and not dm.all()
+        assert_capacity_layer_close(y, oref["y"], dm, name)

@@ -21,8 +21,8 @@ from oracle import moe_oracle as O
 from workloads import SHAPES, MoEShape, make_inputs
 from workloads.generate import to_f64
 
-from gpu_util import (MARGIN, assert_layer_close, biased_margins, np_f, np_i, oracle_layer,
-                      same_sets)
+from gpu_util import (MARGIN, assert_layer_close, biased_margins, check_tokens,
+                      library_routing, np_f, np_i, oracle_layer, same_sets)
 
 pytestmark = pytest.mark.gpu
 
@@ -172,20 +172,37 @@ def test_full_size_dsv3_noaux_sampled():
     cfg = moe.config_from_shape(s)
     ws = moe.Workspace(cfg)
     out = moe.layer_forward(cfg, inp["x"], moe.LayerWeights.from_inputs(inp), ws=ws)
+    lib = library_routing(cfg, inp, ws)
     torch.cuda.synchronize()
     assert moe.moe_get_error(ws) == 0
-    z = O.router_logits(to_f64(inp["x"]), to_f64(inp["w_router"]))
-    ref = O.route(z, s.k, s.gate, s.renormalize, s.rsf, None,
-                  score_bias=to_f64(inp["score_bias"]), n_group=s.n_group,
-                  topk_group=s.topk_group)
+    assert torch.equal(lib["topk_idx"], out["topk_idx"])
     gi = np_i(out["topk_idx"])
-    clear, same = _end_to_end_clear(s, inp, ref, gi)
-    assert np.all(same[clear])
-    assert same.mean() > 0.97
+    b64 = to_f64(inp["score_bias"])
+    # from the library's fp32 logits: key-margin-clear tokens choose the same
+    # experts in the same order
+    zl = np_f(lib["logits"])
+    ref = O.route(zl, s.k, s.gate, s.renormalize, s.rsf, None, score_bias=b64,
+                  n_group=s.n_group, topk_group=s.topk_group)
+    km = biased_margins(ref["scores"], b64, ref["topk_idx"], s.n_group, s.topk_group)
+    np.testing.assert_array_equal(gi[km > KEY_MARGIN], ref["topk_idx"][km > KEY_MARGIN])
+    # end to end from float64 logits
+    z = O.router_logits(to_f64(inp["x"]), to_f64(inp["w_router"]))
+    ref_b = O.route(z, s.k, s.gate, s.renormalize, s.rsf, None, score_bias=b64,
+                    n_group=s.n_group, topk_group=s.topk_group)
+    clear, same_b = _end_to_end_clear(s, inp, ref_b, gi)
+    assert np.all(same_b[clear])
+    assert same_b.mean() > 0.97
     gs = s.E // s.n_group
     assert all(len(set((gi[t] // gs).tolist())) <= s.topk_group for t in range(s.T))
     np.testing.assert_allclose(np_f(out["mean_prob"]), ref["mean_prob"], atol=1e-4)
-    rng = np.random.default_rng(0)
-    pick = np.sort(rng.choice(np.arange(s.T)[same], 24, replace=False))
-    oref = oracle_layer(s, inp, tokens=pick)
+    # outputs of every expert's ragged-tail token (from the library's own
+    # dispatch) and random tokens, among those routed like the oracle
+    same = same_sets(gi, ref["topk_idx"])
+    assert same.mean() > 0.99
+    disp = {"offsets": np_i(lib["offsets"]), "perm": np_i(lib["perm"]),
+            "drop_mask": np_i(lib["drop_mask"])[: s.T * s.k]}
+    pick = check_tokens(disp, s.T, s.k, 320)
+    pick = pick[same[pick]]
+    assert len(pick) >= 300
+    oref = oracle_layer(s, inp, tokens=pick, logits=zl)
     assert_layer_close(np_f(out["y"])[pick], oref["y"], "dsv3 noaux")

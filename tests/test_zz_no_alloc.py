@@ -88,3 +88,31 @@ def test_no_workspace_dispatch_rejects_oversize_batch():
     st = lib.moe_dispatch_no_workspace(ctypes.byref(cfg), fake, fake, fake, fake, fake, fake,
                                        None)
     assert st == B.MOE_ERR_UNSUPPORTED
+
+
+def test_no_workspace_dispatch_out_of_range_index_is_dropped():
+    # With no status word, an expert index outside [0, E) is counted nowhere
+    # and its assignment is marked dropped; the valid assignments dispatch as
+    # moe_dispatch dispatches them (which also records the bad index in its
+    # workspace status word).
+    cfg = moe.make_config(1000, 64, 16, 2, 128, capacity=150)
+    idx = _idx(cfg.T, cfg.n_experts, cfg.top_k, 5, 1.0)
+    bad = [(3, 0, cfg.n_experts), (700, 1, -1)]      # (token, choice, index)
+    for t, j, e in bad:
+        idx[t, j] = e
+    got = _no_workspace(cfg, idx)
+    ws = moe.Workspace(cfg)
+    want = _outputs(cfg)
+    moe.moe_dispatch(cfg, idx, want["counts"], want["drops"], want["offsets"], want["perm"],
+                     want["drop_mask"], ws)
+    torch.cuda.synchronize()
+    A = cfg.T * cfg.top_k
+    for key in ("counts", "drops", "offsets", "drop_mask"):
+        assert torch.equal(got[key], want[key]), key
+    n = int(got["offsets"][-1].item())
+    assert torch.equal(got["perm"][:n], want["perm"][:n])
+    assert int(got["counts"].sum() + got["drops"].sum()) == A - len(bad)
+    for t, j, _ in bad:
+        assert int(got["drop_mask"][t * cfg.top_k + j].item()) == 1
+        assert not bool((got["perm"][:n] == t * cfg.top_k + j).any())
+    assert moe.moe_get_error(ws) == B.MOE_ERR_DEVICE

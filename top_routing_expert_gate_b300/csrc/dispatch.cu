@@ -16,8 +16,6 @@
 // lane rank), so every output is a pure function of topk_idx.
 #include "internal.cuh"
 
-#include <mutex>
-
 namespace moe {
 namespace {
 
@@ -353,37 +351,26 @@ cudaError_t launch_combine(const moe_config_t& c, const float* y_perm, const flo
 // base, each [blocks, E] int32) live in one fixed device array compiled into
 // this library instead of in the caller's workspace.  Every GPU that loads
 // the library holds this array (64 KiB) until the process exits.  Host code
-// cannot use the array's name as a device address, so its address is looked
-// up once per device with cudaGetSymbolAddress and then passed to the
-// kernels like any other pointer.
+// cannot use the array's name as a device address, so every call looks the
+// address up on the current device with cudaGetSymbolAddress (a host-side
+// lookup) and passes it to the kernels like any other pointer.  Looking it up
+// each time, rather than caching it, keeps it right after a cudaDeviceReset,
+// which reloads the library's device code and may move the array.
 // ---------------------------------------------------------------------------
 namespace moe {
 namespace {
 
 constexpr int kStaticDispatchBlocks = 32;   // 32 x 4096 = 131072 assignments
 constexpr int kStaticScratchInts = 2 * kStaticDispatchBlocks * kMaxExperts;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) int32_t g_dispatch_scratch[kStaticScratchInts];
 
-std::mutex g_scratch_mu;
-int32_t* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of g_dispatch_scratch on the current device (looked up on
-// the first call per device).
+// Device address of g_dispatch_scratch on the current device.
 cudaError_t static_scratch(int32_t** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = static_cast<int32_t*>(p);
-  }
-  *out = g_scratch_addr[dev];
+  *out = static_cast<int32_t*>(p);
   return cudaSuccess;
 }
 
@@ -398,11 +385,11 @@ extern "C" moe_status_t moe_dispatch_no_workspace(const moe_config_t* cfg,
                                                   int32_t* perm, uint8_t* drop_mask,
                                                   void* stream) {
   using namespace moe;
-  if (!cfg) return MOE_ERR_INVALID_ARG;
+  // the configuration rules of moe_dispatch, then this entry point's limit
+  const moe_status_t st = validate_config(cfg);
+  if (st != MOE_OK) return st;
   const moe_config_t& c = *cfg;
-  if (c.T < 0 || c.n_experts < 1 || c.top_k < 1 || c.top_k > c.n_experts)
-    return MOE_ERR_INVALID_ARG;
-  if (c.n_experts > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (c.routing != MOE_ROUTE_TOKEN_CHOICE) return MOE_ERR_INVALID_ARG;
   const long long A = (long long)c.T * c.top_k;
   if (A > (long long)kStaticDispatchBlocks * kDispatchChunk) return MOE_ERR_UNSUPPORTED;
   if (!counts || !drops || !offsets || !aligned16_ptr(counts) || !aligned16_ptr(drops) ||

@@ -60,6 +60,10 @@ struct WsLayout {
 
 WsLayout ws_layout(const moe_config_t& c);
 
+// The shape and option rules every entry point applies to a configuration
+// (MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED).
+moe_status_t validate_config(const moe_config_t* c);
+
 // Tokens each expert takes under expert-choice routing (at most T).
 inline int ec_capacity(const moe_config_t& c) {
   long long C = c.capacity >= 0 ? (long long)c.capacity

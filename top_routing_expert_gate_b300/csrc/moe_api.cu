@@ -212,6 +212,8 @@ moe_status_t check_shared_args(const moe_config_t* c, const void* g, const void*
 
 }  // namespace
 
+moe_status_t moe::validate_config(const moe_config_t* c) { return check_config(c); }
+
 extern "C" {
 
 int32_t moe_version(void) { return 500; }
