@@ -1,7 +1,8 @@
 #!/usr/bin/env python
 """MoE layer forward throughput on B300 (one JSON line on rank 0).
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                [--per-config A,B,...] [--impl ours|reference]
 
 A step is one full moe_layer_forward (router, gating/top-k, capacity/dispatch,
 gather, grouped gate/up + SwiGLU, grouped down, combine) over one batch of
@@ -9,9 +10,17 @@ synthetic inputs that are already resident in HBM.  ``value`` is tokens/s over
 all ranks; with N > 1 every rank runs an independent replica (the layer shards
 by tokens with no exchange), so scaling is weak.
 
+The headline is the DeepSeek-V3-shaped prefill layer, the largest layer that
+fits one GPU (its GEMMs are the tensor-bound half of the metric).  The line's
+``per_config`` object carries the same measurement for the Mixtral-shaped
+layer, the DeepSeek-V3-shaped decode layer (the HBM-bound half) and the
+Switch-shaped capacity layer.  Every configuration reports the K-step figure
+(burst clocks) and, under ``sustained``, a seconds-long loop of the same step
+that runs into the power cap, against the sustained tensor peak.
+
 --impl reference times the float64 CPU oracle (the only reference
 implementation: the pages print no code) on the host cores, on a bounded
-sample of the same workload.
+sample of the headline workload.
 """
 
 from __future__ import annotations
@@ -61,17 +70,26 @@ WORKLOAD_TEXT = {
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
+HEADLINE = "dsv3_prefill"
+PER_CONFIG = ("mixtral", "dsv3_decode", "switch")
+
+
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="mixtral", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--per-config", default=",".join(PER_CONFIG),
+                    help="comma-separated workloads measured after the headline one and "
+                         "reported under per_config ('' for none)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample-tokens", type=int, default=16)
     ap.add_argument("--cpu-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--sustain-ms", type=float, default=2000.0,
+                    help="length of the sustained (power-capped) loop per workload; 0 skips it")
     ap.add_argument("--experts", type=int, default=None,
                     help="profiling aid: keep the workload's per-expert GEMM shapes but use "
                          "this many experts (tokens scaled to keep rows per expert)")
@@ -235,37 +253,86 @@ def algorithmic_work(shape, counts):
 # float64 oracle timing (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
 
-def time_oracle(shape, inputs, sample_tokens: int, steps: int, warmup: int = 0):
-    """Oracle forward on the host: routing of all T tokens and the layer output
-    of ``sample_tokens`` tokens per step.  Expert weights are widened to f64 once
-    before timing (resident, as the GPU's weights are resident in HBM)."""
+def oracle_samples(shape, sample_tokens: int, n: int, seed: int = 0):
+    """The token sample of each oracle step (sorted token ids)."""
     import numpy as np
-    import torch
-    from oracle import moe_oracle as O
+    rng = np.random.default_rng(seed)
+    m = min(sample_tokens, shape.T)
+    return [np.sort(rng.choice(shape.T, size=m, replace=False)) for _ in range(n)]
+
+
+def _oracle_inputs(shape, inputs):
     from workloads.generate import to_f64
+    return (to_f64(inputs["x"]), to_f64(inputs["w_router"]), to_f64(inputs["router_bias"]),
+            to_f64(inputs.get("score_bias")), to_f64(inputs.get("shared_gate")))
 
-    x = to_f64(inputs["x"])
-    wr = to_f64(inputs["w_router"])
-    bias = to_f64(inputs["router_bias"])
-    E = shape.E
 
-    def widen(key, e=None):
-        t = inputs[key] if e is None else inputs[key][e]
-        if inputs.get(key + "_scale") is None:
-            return to_f64(t)
-        s = inputs[key + "_scale"] if e is None else inputs[key + "_scale"][e]
-        codes = t.detach().contiguous().view(torch.uint8).cpu().numpy()
-        return O.dequantize_rows(codes, to_f64(s))
+def experts_reached(shape, inputs, samples):
+    """Routed experts whose weights the sampled tokens' outputs use (one
+    untimed routing pass of the oracle over the whole batch)."""
+    import numpy as np
+    from oracle import moe_oracle as O
+    x, wr, bias, sbias, _ = _oracle_inputs(shape, inputs)
+    toks = np.unique(np.concatenate(samples))
+    z = O.router_logits(x, wr, bias)
+    if getattr(shape, "routing", "token") == "expert":
+        C = O.expert_choice_capacity(shape.T, shape.E, shape.k)
+        ec = O.expert_choice(O.gate_scores(z, shape.gate), C)
+        return [e for e in range(shape.E) if np.isin(ec["tokens"][e], toks).any()]
+    r = O.route(z, shape.k, shape.gate, shape.renormalize, shape.rsf,
+                O.expert_capacity(shape.T, shape.E, shape.capacity_factor), score_bias=sbias,
+                n_group=max(shape.n_group, 1), topk_group=shape.topk_group)
+    kept = r["drop_mask"].reshape(shape.T, shape.k)[toks] == 0
+    return sorted(set(r["topk_idx"][toks][kept].tolist()))
 
-    experts = [(widen("w_gate", e), widen("w_up", e), widen("w_down", e)) for e in range(E)]
-    shared = None
-    if inputs.get("ws_gate") is not None:
-        shared = (widen("ws_gate"), widen("ws_up"), widen("ws_down"))
+
+class WidenedExperts:
+    """Float64 expert weights for the oracle, widened once before timing and
+    kept resident on the host (as the GPU's weights are resident in HBM).
+    Only experts some sampled token reaches are widened; a workload with the
+    same weight tensors (same shapes and seed) reuses what is already here."""
+
+    def __init__(self):
+        self.key = None
+        self.experts = {}
+        self.shared = None
+
+    def prepare(self, shape, inputs, needed):
+        import torch
+        from oracle import moe_oracle as O
+        from workloads.generate import to_f64
+        key = (shape.d, shape.E, shape.F, shape.F_s, shape.dtype,
+               getattr(shape, "weight_format", "act"))
+        if key != self.key:
+            self.key, self.experts, self.shared = key, {}, None
+
+        def widen(name, e=None):
+            t = inputs[name] if e is None else inputs[name][e]
+            if inputs.get(name + "_scale") is None:
+                return to_f64(t)
+            sc = inputs[name + "_scale"] if e is None else inputs[name + "_scale"][e]
+            codes = t.detach().contiguous().view(torch.uint8).cpu().numpy()
+            return O.dequantize_rows(codes, to_f64(sc))
+
+        for e in needed:
+            if e not in self.experts:
+                self.experts[e] = (widen("w_gate", e), widen("w_up", e), widen("w_down", e))
+        if inputs.get("ws_gate") is not None and self.shared is None:
+            self.shared = (widen("ws_gate"), widen("ws_up"), widen("ws_down"))
+        return self.experts, (self.shared if inputs.get("ws_gate") is not None else None)
+
+
+def time_oracle(shape, inputs, samples, warmup: int = 0, cache: Optional[WidenedExperts] = None):
+    """Oracle forward on the host, one step per token sample: routing of all
+    T tokens and the layer output of the sampled tokens.  Returns the times of
+    the steps after ``warmup``."""
+    from oracle import moe_oracle as O
+    cache = cache or WidenedExperts()
+    experts, shared = cache.prepare(shape, inputs, experts_reached(shape, inputs, samples))
+    x, wr, bias, sbias, sgate = _oracle_inputs(shape, inputs)
     cap = O.expert_capacity(shape.T, shape.E, shape.capacity_factor)
-    rng = np.random.default_rng(0)
     times = []
-    for i in range(warmup + steps):
-        toks = np.sort(rng.choice(shape.T, size=min(sample_tokens, shape.T), replace=False))
+    for i, toks in enumerate(samples):
         t0 = time.perf_counter()
         if getattr(shape, "routing", "token") == "expert":
             O.moe_layer_expert_choice(x, wr, experts,
@@ -275,9 +342,8 @@ def time_oracle(shape, inputs, sample_tokens: int, steps: int, warmup: int = 0):
             O.moe_layer_forward(x, wr, experts, k=shape.k, gate=shape.gate,
                                 renormalize=shape.renormalize, routed_scaling_factor=shape.rsf,
                                 capacity=cap, router_bias=bias, shared=shared, tokens=toks,
-                                score_bias=to_f64(inputs.get("score_bias")),
-                                n_group=max(shape.n_group, 1), topk_group=shape.topk_group,
-                                shared_gate=to_f64(inputs.get("shared_gate")))
+                                score_bias=sbias, n_group=max(shape.n_group, 1),
+                                topk_group=shape.topk_group, shared_gate=sgate)
         if i >= warmup:
             times.append(time.perf_counter() - t0)
     return times
@@ -317,8 +383,8 @@ def cores_available():
         return os.cpu_count() or 1
 
 
-def timed_oracle(shape, inputs, sample_tokens: int, steps: int, warmup: int = 0,
-                 threads: Optional[int] = None):
+def timed_oracle(shape, inputs, samples, warmup: int = 0, threads: Optional[int] = None,
+                 cache: Optional[WidenedExperts] = None):
     """Oracle timing with the BLAS pools limited to `threads` (default: every
     core of this process's affinity); returns the step times and the BLAS
     threads in effect while they ran.  Without threadpoolctl the BLAS
@@ -327,11 +393,11 @@ def timed_oracle(shape, inputs, sample_tokens: int, steps: int, warmup: int = 0,
     try:
         from threadpoolctl import threadpool_info, threadpool_limits
     except ImportError:
-        return time_oracle(shape, inputs, sample_tokens, steps, warmup), n
+        return time_oracle(shape, inputs, samples, warmup, cache), n
     with threadpool_limits(limits=n, user_api="blas"):
         used = max([p["num_threads"] for p in threadpool_info() if p["user_api"] == "blas"]
                    or [1])
-        times = time_oracle(shape, inputs, sample_tokens, steps, warmup)
+        times = time_oracle(shape, inputs, samples, warmup, cache)
     return times, used
 
 
@@ -339,56 +405,61 @@ def timed_oracle(shape, inputs, sample_tokens: int, steps: int, warmup: int = 0,
 # main
 # ---------------------------------------------------------------------------
 
-def main(argv=None):
-    args = parse_args(argv)
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+def workload_shape(name: str, experts: Optional[int] = None):
+    from workloads import SHAPES
+    shape = SHAPES[name]
+    if experts is not None and experts != shape.E:
+        from dataclasses import replace
+        T = max(1, shape.T * experts // shape.E)
+        shape = replace(shape, name=f"{shape.name}_E{experts}", E=experts,
+                        k=min(shape.k, experts), T=T)
+    return shape
 
+
+def roofline(work, stage_ms, peaks, peak_src, tensor_key, peak_note):
+    """Roofline record of the dominant (longest) stage: its bound is the roof
+    its algorithmic work reaches first (FLOPs at the tensor peak vs bytes at
+    the copy bandwidth): tensor for the prefill GEMMs, HBM for decode and for
+    the Switch layer's few kept tokens over many touched experts."""
+    dom = max(stage_ms, key=stage_ms.get)
+    if tensor_bound(work, dom, peaks, tensor_key):
+        flops = work["flops_gate_up"] if dom == "gate_up" else work["flops_down"]
+        achieved = flops / (stage_ms[dom] * 1e-3) / 1e12
+        peak = peaks[tensor_key]
+        return {"bound": "tensor", "kernel": f"grouped_{dom}", "stage": dom,
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{tensor_key} ({peak_src}; {peak_note})"}
+    nbytes = work["bytes_gate_up"] if dom == "gate_up" else (
+        work["bytes_down"] if dom == "down" else work["weight_bytes"])
+    achieved = nbytes / (stage_ms[dom] * 1e-3) / 1e9
+    peak = peaks["hbm_gbs"]
+    return {"bound": "hbm", "kernel": f"grouped_{dom}" if dom in ("gate_up", "down") else dom,
+            "stage": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_source": f"hbm_gbs ({peak_src})"}
+
+
+def layer_rates(work, ms_per_step, peaks, tensor_key):
+    sec = ms_per_step * 1e-3
+    return {"tflops": work["flops"] / sec / 1e12,
+            # whole layer against the same tensor peak as the roofline
+            "tensor_peak_frac": work["flops"] / sec / 1e12 / peaks[tensor_key],
+            "weight_gbs": work["weight_bytes"] / sec / 1e9,
+            # whole layer's weight stream against the measured copy bandwidth
+            "hbm_frac": work["weight_bytes"] / sec / 1e9 / peaks["hbm_gbs"]}
+
+
+def measure_workload(name, args, dev, world, rank, peaks, peak_src, oracle_cache):
+    """One workload on this rank: warm-up, K timed steps, the sustained loop,
+    the end-to-end leg and (rank 0, one GPU) the oracle baseline.  Returns the
+    record rank 0 reports (None on other ranks)."""
     import torch
     import torch.distributed as dist
 
-    from workloads import SHAPES, make_inputs
-
-    shape = SHAPES[args.workload]
-    if args.experts is not None and args.experts != shape.E:
-        from dataclasses import replace
-        T = max(1, shape.T * args.experts // shape.E)
-        shape = replace(shape, name=f"{shape.name}_E{args.experts}", E=args.experts,
-                        k=min(shape.k, args.experts), T=T)
-
-    if args.impl == "reference":
-        if rank != 0:
-            return 0
-        if torch.cuda.is_available():
-            torch.cuda.set_device(local_rank)
-        dev = "cuda" if torch.cuda.is_available() else "cpu"
-        inputs = make_inputs(shape, device=dev, seed=0)
-        times, used = timed_oracle(shape, inputs, args.cpu_sample_tokens, args.steps, args.warmup)
-        t = statistics.mean(times)
-        val = args.cpu_sample_tokens / t
-        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
-                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": 1e3 * t, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": WORKLOAD_TEXT[args.workload], "name": shape.name},
-                "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": used,
-                                 "kind": "oracle",
-                                 "sample": f"per step: routing of all {shape.T} tokens + layer "
-                                           f"output of {args.cpu_sample_tokens} sampled tokens"},
-                "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
-                        "d2h_bytes_per_step": 0}}
-        print(json.dumps(line), flush=True)
-        return 0
-
     import top_routing_expert_gate_b300 as moe
     from top_routing_expert_gate_b300 import _binding as B
+    from workloads import make_inputs
 
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-
+    shape = workload_shape(name, args.experts)
     inputs = make_inputs(shape, device=dev, seed=0)
     cfg = moe.config_from_shape(shape, out_dtype="fp32")
     ws = moe.Workspace(cfg, dev)
@@ -411,53 +482,66 @@ def main(argv=None):
             e.record(stream)      # creates the underlying cudaEvent
         return evs
 
-    step_events = [new_events(NS + 1) for _ in range(args.steps)]
-    warm_events = new_events(NS + 1)
-
     def step(evs):
         return moe.moe_layer_forward_profiled(cfg, x, w.w_router, w.router_bias, w.score_bias,
                                               w.w_gate, w.w_up, w.w_down, w.ws_gate, w.ws_up,
                                               w.ws_down, w.shared_gate, w.scales, y, topk_idx,
                                               topk_w, counts, drops, mean_prob, ws, evs, stream)
 
+    warm_events = new_events(NS + 1)
     for _ in range(args.warmup):
         step(warm_events)
     torch.cuda.synchronize(dev)
-    status = moe.moe_get_error(ws)
-    if status != 0:
-        raise RuntimeError(f"device status {status} after warm-up")
-    counts_host = counts.cpu().tolist()
-    work = algorithmic_work(shape, counts_host)
+    if moe.moe_get_error(ws) != 0:
+        raise RuntimeError(f"{name}: device status after warm-up")
+    work = algorithmic_work(shape, counts.cpu().tolist())
 
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    launches = 0
-    clocks.mark_begin()
-    t_start.record(stream)
-    for i in range(args.steps):
-        launches += step(step_events[i])
-    t_end.record(stream)
-    torch.cuda.synchronize(dev)
-    clocks.mark_end()
-    if world > 1:
-        dist.barrier()
-    clocks.stop()
-    total_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
-    ms_per_step = total_ms / args.steps
-    status = moe.moe_get_error(ws)
-    if status != 0:
-        raise RuntimeError(f"device status {status} after the timed steps")
+    def timed_loop(n_steps):
+        """n_steps layer calls between a barrier + synchronize on both sides;
+        returns (ms per step over the slowest rank, per-stage ms, launches,
+        clock summary)."""
+        evs = [new_events(NS + 1) for _ in range(n_steps)]
+        clocks = ClockSampler(dev.index if dev.index is not None else 0)
+        clocks.start()
+        time.sleep(0.3)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        launches = 0
+        clocks.mark_begin()
+        t0.record(stream)
+        for i in range(n_steps):
+            launches += step(evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        clocks.mark_end()
+        if world > 1:
+            dist.barrier()
+        clocks.stop()
+        ms = max_over_ranks(t0.elapsed_time(t1), dev) / n_steps
+        if moe.moe_get_error(ws) != 0:
+            raise RuntimeError(f"{name}: device status after the timed steps")
+        stage = {}
+        for si, sname in enumerate(B.STAGE_NAMES):
+            vals = [ev[si].elapsed_time(ev[si + 1]) for ev in evs]
+            stage[sname] = sum(vals) / len(vals)
+        return ms, stage, launches, clocks.summary()
 
-    stage_ms = {}
-    for si, name in enumerate(B.STAGE_NAMES):
-        vals = [ev[si].elapsed_time(ev[si + 1]) for ev in step_events]
-        stage_ms[name] = sum(vals) / len(vals)
+    ms_per_step, stage_ms, launches, clk = timed_loop(args.steps)
+
+    # a seconds-long loop of the same step, long enough to reach the power cap
+    sustained = None
+    if args.sustain_ms > 0:
+        n_sus = max(args.steps, int(math.ceil(args.sustain_ms / ms_per_step)))
+        s_ms, s_stage, _, s_clk = timed_loop(n_sus)
+        s_key = "bf16_tflops_sustained" if "bf16_tflops_sustained" in peaks else "bf16_tflops"
+        sustained = {"value": tokens_per_second(T, world, s_ms), "unit": "tokens/s",
+                     "ms_per_step": s_ms, "steps": n_sus, "stage_ms": s_stage,
+                     "roofline": roofline(work, s_stage, peaks, peak_src, s_key,
+                                          "seconds-long loop"),
+                     **layer_rates(work, s_ms, peaks, s_key), "clocks": s_clk}
 
     # end to end through the C ABI's host-buffer call: every step copies its
     # x from pinned host memory, runs the layer and copies y back.  Two
@@ -482,6 +566,8 @@ def main(argv=None):
     for i in range(2 * n_pipe):
         e2e_step(i)
     torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
     e2e_start.record(stream)
     for p in pipes:
         p["stream"].wait_event(e2e_start)
@@ -494,88 +580,134 @@ def main(argv=None):
     e2e_ms = max_over_ranks(e2e_start.elapsed_time(e2e_end) / args.e2e_steps, dev)
     for p in pipes[1:]:
         if moe.moe_get_error(p["ws"]) != 0:
-            raise RuntimeError("device status after the end-to-end steps")
+            raise RuntimeError(f"{name}: device status after the end-to-end steps")
 
+    record = None
+    if rank == 0:
+        # A timed loop that ran into the power cap is compared with the
+        # sustained tensor peak (a seconds-long GEMM loop under the same cap);
+        # otherwise with the burst peak.
+        capped = "sw_power_cap" in clk.get("reasons", []) and "bf16_tflops_sustained" in peaks
+        tensor_key = "bf16_tflops_sustained" if capped else "bf16_tflops"
+        roof = roofline(work, stage_ms, peaks, peak_src, tensor_key,
+                        "power-capped timed loop" if capped else "no power cap seen")
+        # counters of a reduced-expert run do not describe the full workload
+        roof["traffic"] = None if args.experts else stored_traffic(name, roof["stage"])
+        record = {
+            "workload": WORKLOAD_TEXT[name], "name": shape.name,
+            "value": tokens_per_second(T, world, ms_per_step), "unit": "tokens/s",
+            "ms_per_step": ms_per_step, "steps": args.steps, "dtype": shape.dtype,
+            **layer_rates(work, ms_per_step, peaks, tensor_key),
+            "stage_ms": stage_ms, "roofline": roof, "gpu_launches": launches, "clocks": clk,
+            "e2e": {"value": tokens_per_second(T, world, e2e_ms), "unit": "tokens/s",
+                    "h2d_bytes_per_step": x.numel() * x.element_size(),
+                    "d2h_bytes_per_step": y.numel() * y.element_size(),
+                    "api": "moe_layer_forward_host", "batches_in_flight": E2E_PIPELINE},
+            "sustained": sustained,
+            "config": {"workload": WORKLOAD_TEXT[name], "name": shape.name,
+                       "global_batch_tokens": world * T, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2: every step streams "
+                             f"{work['weight_bytes'] / 1e9:.2f} GB of expert weights "
+                             "(L2 126 MB)",
+                       "kept_assignments": work["kept"], "touched_experts": work["touched"]},
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            samples = oracle_samples(shape, args.cpu_sample_tokens, args.cpu_steps)
+            times, used = timed_oracle(shape, inputs, samples, cache=oracle_cache)
+            t = statistics.mean(times)
+            record["cpu_baseline"] = {
+                "value": len(samples[0]) / t, "unit": "tokens/s", "cores": used,
+                "kind": "oracle",
+                "sample": f"{args.cpu_steps} oracle steps, each: routing of all {T} tokens + "
+                          f"layer output of {len(samples[0])} sampled tokens (float64; the "
+                          "experts they reach widened to float64 before timing)"}
+            if name == "tiny":
+                # the small layer's single-thread figure beside the all-core one
+                times1, _ = timed_oracle(shape, inputs, samples, threads=1, cache=oracle_cache)
+                record["cpu_baseline"]["single_thread_value"] = (len(samples[0]) /
+                                                                 statistics.mean(times1))
+    del pipes, inputs, w, ws, x, y
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return record
+
+
+def reference_main(args, rank, local_rank):
+    """The reference arm: the float64 oracle as it stands, timed on the host
+    cores on a bounded sample of the headline workload."""
+    import torch
+    from workloads import make_inputs
     if rank != 0:
-        if world > 1:
-            dist.barrier()
-            dist.destroy_process_group()
         return 0
-
-    peaks, peak_src = load_peaks()
-    clk = clocks.summary()
-    # A timed loop that ran into the power cap is compared with the sustained
-    # tensor peak (a seconds-long GEMM loop under the same cap); otherwise with
-    # the burst peak.
-    sustained = "sw_power_cap" in clk.get("reasons", []) and "bf16_tflops_sustained" in peaks
-    # dominant stage: the longest one; its bound is the roof its algorithmic
-    # work reaches first (FLOPs at the tensor peak vs bytes at the copy
-    # bandwidth): tensor for the prefill GEMMs, HBM for decode and for the
-    # Switch layer's few kept tokens over many touched experts
-    dom = max(stage_ms, key=stage_ms.get)
-    tensor_key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
-    if tensor_bound(work, dom, peaks, tensor_key):
-        flops = work["flops_gate_up"] if dom == "gate_up" else work["flops_down"]
-        achieved = flops / (stage_ms[dom] * 1e-3) / 1e12
-        key = tensor_key
-        peak = peaks[key]
-        roof = {"bound": "tensor", "kernel": f"grouped_{dom}", "achieved": achieved,
-                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": f"{key} ({peak_src}; "
-                               f"{'power-capped timed loop' if sustained else 'no power cap seen'})"}
-    else:
-        nbytes = work["bytes_gate_up"] if dom == "gate_up" else (
-            work["bytes_down"] if dom == "down" else work["weight_bytes"])
-        achieved = nbytes / (stage_ms[dom] * 1e-3) / 1e9
-        peak = peaks["hbm_gbs"]
-        roof = {"bound": "hbm", "kernel": f"grouped_{dom}" if dom in ("gate_up", "down") else dom,
-                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "peak_source": f"hbm_gbs ({peak_src})"}
-    # counters of a reduced-expert run do not describe the full workload
-    roof["traffic"] = None if args.experts else stored_traffic(args.workload, dom)
-
-    value = tokens_per_second(T, world, ms_per_step)
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": shape.dtype,
-        "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": shape.name,
-                   "global_batch_tokens": world * T, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2: every step streams "
-                         f"{work['weight_bytes'] / 1e9:.2f} GB of expert weights (L2 126 MB)",
-                   "kept_assignments": work["kept"], "touched_experts": work["touched"]},
-        "tflops": work["flops"] / (ms_per_step * 1e-3) / 1e12,
-        # whole layer against the same tensor peak as the roofline
-        "tensor_peak_frac": work["flops"] / (ms_per_step * 1e-3) / 1e12 /
-                            peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"],
-        "weight_gbs": work["weight_bytes"] / (ms_per_step * 1e-3) / 1e9,
-        # whole layer's weight stream against the measured copy bandwidth
-        "hbm_frac": work["weight_bytes"] / (ms_per_step * 1e-3) / 1e9 / peaks["hbm_gbs"],
-        "stage_ms": stage_ms,
-        "roofline": roof,
-        "gpu_launches": launches,
-        "clocks": clk,
-        "e2e": {"value": tokens_per_second(T, world, e2e_ms), "unit": "tokens/s",
-                "h2d_bytes_per_step": x.numel() * x.element_size(),
-                "d2h_bytes_per_step": y.numel() * y.element_size(),
-                "api": "moe_layer_forward_host", "batches_in_flight": E2E_PIPELINE},
-    }
-    if world == 1 and not args.no_cpu_baseline:
-        times, used = timed_oracle(shape, inputs, args.cpu_sample_tokens, args.cpu_steps)
-        t = statistics.mean(times)
-        line["cpu_baseline"] = {"value": args.cpu_sample_tokens / t, "unit": "tokens/s",
-                                "cores": used, "kind": "oracle",
-                                "sample": f"{args.cpu_steps} oracle steps, each: routing of all "
-                                          f"{T} tokens + layer output of "
-                                          f"{args.cpu_sample_tokens} sampled tokens"}
-        if args.workload == "tiny":
-            # the small layer's single-thread figure beside the all-core one
-            times1, _ = timed_oracle(shape, inputs, args.cpu_sample_tokens, args.cpu_steps,
-                                     threads=1)
-            line["cpu_baseline"]["single_thread_value"] = (args.cpu_sample_tokens /
-                                                           statistics.mean(times1))
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local_rank)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    shape = workload_shape(args.workload, args.experts)
+    inputs = make_inputs(shape, device=dev, seed=0)
+    samples = oracle_samples(shape, args.cpu_sample_tokens, args.warmup + args.steps)
+    times, used = timed_oracle(shape, inputs, samples, args.warmup)
+    t = statistics.mean(times)
+    m = len(samples[0])
+    val = m / t
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.workload], "name": shape.name},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                             "sample": f"per step: routing of all {shape.T} tokens + layer "
+                                       f"output of {m} sampled tokens"},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return reference_main(args, rank, local_rank)
+
+    import torch
+    import torch.distributed as dist
+
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks, peak_src = load_peaks()
+    cache = WidenedExperts()
+
+    names = [args.workload] + [n for n in args.per_config.split(",")
+                               if n and n != args.workload]
+    for n in names:
+        if n not in WORKLOAD_TEXT:
+            raise SystemExit(f"unknown workload {n!r}")
+    records = {}
+    for n in names:
+        records[n] = measure_workload(n, args, dev, world, rank, peaks, peak_src, cache)
+
+    if rank == 0:
+        head = records[args.workload]
+        line = {
+            "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": head["dtype"],
+            "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
+            "config": head["config"],
+            **{k: head[k] for k in ("tflops", "tensor_peak_frac", "weight_gbs", "hbm_frac",
+                                    "stage_ms", "roofline", "gpu_launches", "clocks", "e2e",
+                                    "sustained")},
+        }
+        if "cpu_baseline" in head:
+            line["cpu_baseline"] = head["cpu_baseline"]
+        line["per_config"] = {n: records[n] for n in names[1:]}
+        print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
