@@ -501,9 +501,11 @@ def switch_balance_term(f: np.ndarray, P: np.ndarray) -> float:
 # largest finite value is 448.
 # ---------------------------------------------------------------------------
 
-def e4m3_to_f64(codes) -> np.ndarray:
-    """Value of each E4M3 code (uint8 array), straight from the format."""
-    c = np.asarray(codes, dtype=np.int64)
+def _e4m3_value(c: np.ndarray) -> np.ndarray:
+    """Value of each E4M3 code, straight from the format: sign bit, 4-bit
+    exponent of bias 7, 3-bit mantissa; exponent 0 is subnormal (m * 2^-9);
+    S.1111.111 is NaN."""
+    c = np.asarray(c, dtype=np.int64)
     sign = np.where((c >> 7) & 1, -1.0, 1.0)
     e = (c >> 3) & 0xF
     m = (c & 0x7).astype(np.float64)
@@ -511,6 +513,16 @@ def e4m3_to_f64(codes) -> np.ndarray:
     sub = m * 2.0 ** -9
     v = sign * np.where(e == 0, sub, normal)
     return np.where((e == 15) & ((c & 7) == 7), np.nan, v)
+
+
+# the definition above evaluated once for every one of the 256 codes
+_E4M3_VALUES = _e4m3_value(np.arange(256))
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Value of each E4M3 code (uint8 array): the format's definition
+    (``_e4m3_value``), looked up per code."""
+    return _E4M3_VALUES[np.asarray(codes, dtype=np.uint8)]
 
 
 def dequantize_rows(codes, scale) -> np.ndarray:

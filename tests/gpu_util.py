@@ -37,15 +37,20 @@ def assert_layer_close(y_gpu: np.ndarray, y_ref: np.ndarray, what: str = "y"):
 
 def assert_capacity_layer_close(y_gpu: np.ndarray, y_ref: np.ndarray, drop_mask: np.ndarray,
                                 what: str = "y"):
-    """With a capacity: tokens whose every choice was dropped must equal the
-    reference exactly (0, or the shared expert's output), and the others are
-    held to the layer tolerance relative to their own RMS (the dropped
-    tokens' exact zeros would otherwise deflate the RMS of the comparison)."""
+    """With a capacity: tokens whose every choice was dropped must be exactly
+    zero without a shared expert; with one they carry only the shared
+    expert's output, held to the layer tolerance relative to their own RMS.
+    The other tokens are held to the layer tolerance relative to their own
+    RMS (the dropped tokens' exact zeros would otherwise deflate the RMS of
+    the comparison)."""
     y_gpu = np.asarray(y_gpu, dtype=np.float64)
     y_ref = np.asarray(y_ref, dtype=np.float64)
     all_dropped = np.all(np.asarray(drop_mask).reshape(y_ref.shape[0], -1) != 0, axis=1)
     if all_dropped.any():
-        np.testing.assert_allclose(y_gpu[all_dropped], y_ref[all_dropped], rtol=2e-3, atol=1e-6)
+        if np.all(y_ref[all_dropped] == 0.0):
+            assert np.all(y_gpu[all_dropped] == 0.0), f"{what}: dropped tokens must be 0"
+        else:
+            assert_layer_close(y_gpu[all_dropped], y_ref[all_dropped], what + " (all dropped)")
     if (~all_dropped).any():
         assert_layer_close(y_gpu[~all_dropped], y_ref[~all_dropped], what)
 

@@ -61,6 +61,12 @@ MID_SHAPES = {
     # N tail (d = 320 is one full 256-column tile plus 64 columns)
     "mid_multi_mtile": _shape(T=1000, d=320, E=4, k=2, F=256, F_s=128),
     "mid_wide_ff": _shape(T=520, d=128, E=3, k=1, F=1024, gate="sigmoid", rsf=2.5),
+    # 257..288 rows in one group: the weights-in-M kernel runs such a tile as
+    # two MMAs over both tensor-memory accumulators (every routed expert and
+    # the shared expert here; the second shape sits on the 288-row edge with a
+    # down-projection N tail)
+    "mid_big_tiles": _shape(T=270, d=256, E=2, k=2, F=256, F_s=128, gate="sigmoid", rsf=2.5),
+    "mid_big_tile_edge": _shape(T=288, d=320, E=3, k=3, F=128, F_s=128),
     # the shared expert behind a per-token sigmoid gate
     "mid_gated_shared": _shape(T=333, d=256, E=16, k=4, F=256, F_s=256, gate="sigmoid",
                                rsf=2.5, shared_gate=True),

@@ -11,10 +11,14 @@
 // computed transposed, D^T = W . X^T: MMA rows (TMEM lanes) are output
 // features of one expert and the MMA's N columns are that expert's tokens.
 // tcgen05 takes any N that is a multiple of 16 up to 256, so an expert with
-// R rows is covered by ceil(R / 256) token tiles of round32(R / tiles)
-// columns each: the padding is below 32 rows per tile, where 128-row token
-// tiles waste up to 127 (about a fifth of the work when every expert holds
-// ~256 rows, as in the DeepSeek-V3-shaped layer).
+// R <= 256 rows is one token tile of round32(R) columns: the padding is below
+// 32 rows, where 128-row token tiles waste up to 127 (about a fifth of the
+// work when every expert holds ~256 rows, as in the DeepSeek-V3-shaped
+// layer).  An expert with 256 < R <= 288 rows is still one token tile: two
+// MMAs per K step (N = 256, then the last round32(R) - 256 tokens) into one
+// accumulator spanning both halves of tensor memory, so no other pair has to
+// stream the same weight tile.  Larger experts are split into
+// ceil(R / 256) tiles of round32(R / tiles) columns.
 //
 // Two CTAs (a cluster pair, on two SMs) share one M = 256 MMA
 // (tcgen05 .cta_group::2): each CTA stages its own 128 weight rows and half
@@ -28,8 +32,9 @@
 //               CTAs completes on the even CTA's stage barrier;
 //   warp 1      allocates 512 TMEM columns (pair allocation); in the even CTA
 //               one thread issues tcgen05.mma.cta_group::2 M=256 N=N K=16
-//               into one of two 256-column fp32 accumulators and multicasts
-//               stage-free / accumulator-full commits to both CTAs;
+//               into one of two 256-column fp32 accumulators (a tile of more
+//               than 256 tokens takes both) and multicasts stage-free /
+//               accumulator-full commits to both CTAs;
 //   warps 2..5  epilogue on this CTA's 128 lanes (= 128 features, all N
 //               tokens).  Gate/up: the warps holding W_gate lanes and those
 //               holding the matching W_up lanes swap half of each 32-token
@@ -46,11 +51,13 @@ using namespace tc;
 
 constexpr int WM = 128;             // weight rows per CTA (MMA M = 256 per pair)
 constexpr int WBK = 64;             // k-block: one 128-byte swizzle span of bf16
-constexpr int TN = 256;             // maximum token columns per pair tile (MMA N)
-constexpr int TNH = TN / 2;         // token rows staged by each CTA
+constexpr int TN = 256;             // token columns of one MMA (its largest N)
+constexpr int TN_BIG = 288;         // token columns of a tile that takes both accumulators
+constexpr int TNH = TN_BIG / 2;     // token rows staged by each CTA
 constexpr int WSTAGES = 6;
 constexpr uint32_t W_STAGE = WM * WBK * 2;    // 16 KB
-constexpr uint32_t T_STAGE = TNH * WBK * 2;   // 16 KB
+constexpr uint32_t T_STAGE = TNH * WBK * 2;   // 18 KB: 128 rows of the first MMA + 16 of the second
+constexpr uint32_t T_TAIL = (TN / 2) * WBK * 2;   // offset of the second MMA's token rows
 constexpr int kWThreads = 192;
 constexpr uint32_t kWTmemCols = 512;
 constexpr int kWMaxGroups = kMaxExperts + 1;
@@ -100,6 +107,34 @@ __device__ __forceinline__ bool epi_bar_any(bool v) {
   return r != 0;
 }
 
+// The two 256-column accumulators in tensor memory, as the MMA issuer and
+// the epilogue both walk them over the same tile sequence: a tile of at most
+// 256 tokens takes the next buffer in turn, a larger one takes both (columns
+// 0..n).  Each buffer counts its uses, which gives the mbarrier phase to wait
+// for: the release of its previous use (MMA side) or the completion of its
+// current one (epilogue side).
+struct AccBuffers {
+  int next = 0;
+  uint32_t uses0 = 0u, uses1 = 0u;
+  __device__ __forceinline__ void take(bool both, int& b0, int& b1) {
+    if (both) {
+      b0 = 0;
+      b1 = 1;
+    } else {
+      b0 = b1 = next;
+      next ^= 1;
+    }
+  }
+  __device__ __forceinline__ uint32_t uses(int b) const { return b ? uses1 : uses0; }
+  __device__ __forceinline__ uint32_t free_parity(int b) const { return (uses(b) & 1u) ^ 1u; }
+  __device__ __forceinline__ uint32_t full_parity(int b) const { return uses(b) & 1u; }
+  // buffers b0..b1 (b0 <= b1) have been used once more
+  __device__ __forceinline__ void used(int b0, int b1) {
+    if (b0 == 0) ++uses0;
+    if (b1 == 1) ++uses1;
+  }
+};
+
 template <int MODE>
 __global__ void __launch_bounds__(kWThreads, 1)
 grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
@@ -147,7 +182,10 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
     }
     int nt = (rows + TN - 1) / TN;
     int ts = 32;
-    if (nt > 0) {
+    if (rows > TN && rows <= TN_BIG) {
+      nt = 1;                                   // one tile over both accumulators
+      ts = (rows + 31) & ~31;                   // <= TN_BIG
+    } else if (nt > 0) {
       ts = ((rows + nt - 1) / nt + 31) & ~31;   // <= TN
       nt = (rows + ts - 1) / ts;
     }
@@ -231,10 +269,15 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
         tile_rows(g, j, first, rows, n);
         const int kind = g < p.E ? 0 : 1;
         const int nk = p.K[kind] / WBK;
-        const int half = n >> 1;   // token rows staged by this CTA, multiple of 16
+        // token rows staged by this CTA (multiples of 16): its half of the
+        // first MMA's N and, for a tile over 256 tokens, its half of the
+        // second MMA's N, staged T_TAIL bytes in
+        const int n1 = min(n, TN), n2 = n - n1;
+        const int half = n1 >> 1, half2 = n2 >> 1;
         const int w_row = (kind ? 0 : g * p.w_rows_per_expert) + f * fpt + (int)rank * (fpt / 2);
         const int t_row = s_row0[g] + first + (int)rank * half;
-        const uint32_t tx_pair = 2u * (W_STAGE + (uint32_t)half * (WBK * 2));
+        const int t_row2 = s_row0[g] + first + n1 + (int)rank * half2;
+        const uint32_t tx_pair = 2u * W_STAGE + (uint32_t)n * (WBK * 2);
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
             failed = true;
@@ -256,6 +299,16 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
             while (half - off >= box) {
               tma_load_2d_pair(t_dst + (uint32_t)off * (WBK * 2), &p.t_map[kind][b], fb,
                                kb * WBK, t_row + off);
+              off += box;
+            }
+          }
+          off = 0;
+#pragma unroll
+          for (int b = 0; b < kTokBoxes; ++b) {
+            const int box = 128 >> b;
+            while (half2 - off >= box) {
+              tma_load_2d_pair(t_dst + T_TAIL + (uint32_t)off * (WBK * 2), &p.t_map[kind][b],
+                               fb, kb * WBK, t_row2 + off);
               off += box;
             }
           }
@@ -286,22 +339,25 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
       // ---------------- MMA issuer (even CTA) ----------------
       int stage = 0;
       uint32_t phase = 0;
-      int local = 0;
-      for (int t = pair; t < total && !failed; t += npairs, ++local) {
+      AccBuffers acc;
+      for (int t = pair; t < total && !failed; t += npairs) {
         int g, f, j, first, rows, n;
         decode(t, g, f, j);
         tile_rows(g, j, first, rows, n);
         const int kind = g < p.E ? 0 : 1;
         const int nk = p.K[kind] / WBK;
-        const uint32_t idesc = idesc_bf16_f32(2 * WM, (uint32_t)n);
-        const int buf = local & 1;
-        const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
-        if (!mbar_wait_cluster(acce_bar(buf), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
-          failed = true;
-          break;
-        }
+        const int n1 = min(n, TN), n2 = n - n1;
+        const uint32_t idesc1 = idesc_bf16_f32(2 * WM, (uint32_t)n1);
+        const uint32_t idesc2 = idesc_bf16_f32(2 * WM, (uint32_t)(n2 > 0 ? n2 : 32));
+        int b0, b1;
+        acc.take(n > TN, b0, b1);
+        // wait until the epilogue has released every buffer this tile uses
+        for (int b = b0; b <= b1 && !failed; ++b)
+          if (!mbar_wait_cluster(acce_bar(b), acc.free_parity(b), abort_flag, p.timeout_ns))
+            failed = true;
+        if (failed) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * TN);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(b0 * TN);
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait_cluster(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
             failed = true;
@@ -310,11 +366,15 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
           tc_fence_after();
           const uint64_t a_desc = sdesc_k128(sW + stage * W_STAGE);
           const uint64_t b_desc = sdesc_k128(sT + stage * T_STAGE);
+          const uint64_t b_desc2 = sdesc_k128(sT + stage * T_STAGE + T_TAIL);
 #pragma unroll
           for (int kk = 0; kk < WBK / 16; ++kk) {
             // advance 16 bf16 = 32 bytes along K inside the swizzle span
-            mma_bf16_pair(d_tmem, a_desc + (uint64_t)(2 * kk), b_desc + (uint64_t)(2 * kk), idesc,
-                          (kb | kk) != 0 ? 1u : 0u);
+            mma_bf16_pair(d_tmem, a_desc + (uint64_t)(2 * kk), b_desc + (uint64_t)(2 * kk),
+                          idesc1, (kb | kk) != 0 ? 1u : 0u);
+            if (n2 > 0)
+              mma_bf16_pair(d_tmem + (uint32_t)TN, a_desc + (uint64_t)(2 * kk),
+                            b_desc2 + (uint64_t)(2 * kk), idesc2, (kb | kk) != 0 ? 1u : 0u);
           }
           mma_commit_pair_mc(empty_bar(stage), 3);
           if (++stage == WSTAGES) {
@@ -323,7 +383,8 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
           }
         }
         if (failed) break;
-        mma_commit_pair_mc(accf_bar(buf), 3);
+        for (int b = b0; b <= b1; ++b) mma_commit_pair_mc(accf_bar(b), 3);
+        acc.used(b0, b1);
       }
       if (failed) {
         *abort_flag = 1;
@@ -338,16 +399,18 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
     const int q = warp & 3;   // TMEM lane quarter this warp may access
     const uint32_t lead_acce0 = mapa_shared(acce_bar(0), 0);
     const uint32_t lead_acce1 = mapa_shared(acce_bar(1), 0);
-    int local = 0;
+    AccBuffers acc;
     uint32_t chunk_no = 0;    // running count of exchange chunks (buffer parity)
-    for (int t = pair; t < total; t += npairs, ++local) {
+    for (int t = pair; t < total; t += npairs) {
       int g, f, j, first, rows, n;
       decode(t, g, f, j);
       tile_rows(g, j, first, rows, n);
       const int kind = g < p.E ? 0 : 1;
-      const int buf = local & 1;
-      const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
-      const bool ok = mbar_wait_cluster(accf_bar(buf), acc_phase, abort_flag, p.timeout_ns);
+      int b0, b1;
+      acc.take(n > TN, b0, b1);
+      bool ok = true;
+      for (int b = b0; b <= b1; ++b)
+        ok = ok && mbar_wait_cluster(accf_bar(b), acc.full_parity(b), abort_flag, p.timeout_ns);
       if (MODE == kWGateUp) {
         // the exchange below synchronises the four warps, so all of them
         // must take the same decision on whether to process the tile
@@ -360,7 +423,7 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
         break;
       }
       tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * TN);
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b0 * TN);
       const size_t row0 = (size_t)(kind ? 0 : s_row0[g]) + (size_t)first;
       const int feat0 = f * fpt + (int)rank * (fpt / 2);   // this CTA's first feature
       if (MODE == kWGateUp) {
@@ -414,7 +477,9 @@ grouped_gemm_wm_kernel(const __grid_constant__ WmParams p) {
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(buf ? lead_acce1 : lead_acce0);
+      if (lane == 0)
+        for (int b = b0; b <= b1; ++b) mbar_arrive_cluster(b ? lead_acce1 : lead_acce0);
+      acc.used(b0, b1);
     }
     if (failed) {
       *abort_flag = 1;
