@@ -86,14 +86,28 @@ def _layer_and_routing(s, inp, ws=None):
     return cfg, out, lib
 
 
-@pytest.mark.parametrize("layout", ["tokens_m", "weights_m"])
+# the bf16 grouped GEMMs: tokens in the MMA's M with the gather fused into
+# the gate/up kernel (default), the same with the separate gather kernel, and
+# the expert weights in M on CTA pairs
+LAYOUTS = ["tokens_m", "tokens_m_gather_kernel", "weights_m"]
+
+
+def _set_layout(monkeypatch, layout):
+    monkeypatch.setenv("MOE_B300_EXPERT_LAYOUT", layout.replace("_gather_kernel", ""))
+    if layout.endswith("_gather_kernel"):
+        monkeypatch.setenv("MOE_B300_SEPARATE_GATHER", "1")
+    else:
+        monkeypatch.delenv("MOE_B300_SEPARATE_GATHER", raising=False)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
 @pytest.mark.parametrize("name", list(MID_SHAPES))
 def test_layer_matches_oracle_all_tokens(name, layout, monkeypatch):
-    # both tile layouts of the bf16 grouped GEMMs (tokens or weights in the
-    # MMA's M).  The oracle routes from the library's fp32 logits, so (a) the
-    # routing and dispatch arrays must agree bit for bit and (c) the output is
-    # compared on every token, capacity layers included.
-    monkeypatch.setenv("MOE_B300_EXPERT_LAYOUT", layout)
+    # every tile layout of the bf16 grouped GEMMs.  The oracle routes from the
+    # library's fp32 logits, so (a) the routing and dispatch arrays must agree
+    # bit for bit and (c) the output is compared on every token, capacity
+    # layers included.
+    _set_layout(monkeypatch, layout)
     s = MID_SHAPES[name]
     inp = make_inputs(s, device=DEV, seed=1)
     cfg, out, lib = _layer_and_routing(s, inp)

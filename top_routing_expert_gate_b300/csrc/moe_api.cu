@@ -167,10 +167,25 @@ int fp8_tmem_tile(const moe_config_t& c) {
   return (int64_t)c.T * c.top_k <= (int64_t)64 * c.n_experts && c.T <= 256 ? 64 : 128;
 }
 
-cudaError_t run_experts(const moe_config_t& c, const ExpertArgs& a, cudaStream_t s) {
-  if (c.act_dtype != MOE_BF16) return launch_experts_simt(c, a, s);
+// The gather (x_perm[r] = x[perm[r] / div]) and the two grouped GEMMs.  The
+// bf16 tokens-in-M gate/up kernel reads its A rows from x itself, so for it
+// no gather runs and no x_perm is written.
+cudaError_t run_experts(const moe_config_t& c, ExpertArgs a, void* x_perm, cudaStream_t s) {
   const bool fp8 = c.weight_format == MOE_WEIGHTS_FP8_E4M3;
   const int fp8_tn = fp8 ? fp8_tmem_tile(c) : 0;
+  const int div = c.routing == MOE_ROUTE_EXPERT_CHOICE ? 1 : c.top_k;
+  const bool fused_gather =
+      c.act_dtype == MOE_BF16 && !fp8 && !weights_in_m(c, kGemmGateUp) &&
+      getenv("MOE_B300_SEPARATE_GATHER") == nullptr;
+  if (fused_gather) {
+    a.gather_div = div;
+  } else {
+    const cudaError_t e = launch_gather(c, a.x, a.perm, a.offsets, x_perm, a.status, s,
+                                        a.launches, div);
+    if (e != cudaSuccess) return e;
+    a.x_perm = x_perm;
+  }
+  if (c.act_dtype != MOE_BF16) return launch_experts_simt(c, a, s);
   for (int which = kGemmGateUp; which <= kGemmDown; ++which) {
     cudaEvent_t ev = which == kGemmGateUp ? a.ev_up : a.ev_down;
     if (ev) {
@@ -358,12 +373,10 @@ moe_status_t moe_grouped_swiglu(const moe_config_t* cfg, const void* x, const in
   const WsLayout L = ws_layout(*cfg);
   cudaStream_t s = (cudaStream_t)stream;
   int32_t* status = at<int32_t>(ws, L.status);
-  void* x_perm = at<char>(ws, L.x_perm);
-  MOE_TRY_CUDA(launch_gather(*cfg, x, perm, offsets, x_perm, status, s));
   ExpertArgs a{};
   a.x = x;
-  a.x_perm = x_perm;
   a.offsets = offsets;
+  a.perm = perm;
   a.w_gate = w_gate;
   a.w_up = w_up;
   a.w_down = w_down;
@@ -377,7 +390,7 @@ moe_status_t moe_grouped_swiglu(const moe_config_t* cfg, const void* x, const in
   a.status = status;
   a.scales = scales;
   a.rows = (int)grouped_rows(*cfg);
-  return cuda_status(run_experts(*cfg, a, s));
+  return cuda_status(run_experts(*cfg, a, at<char>(ws, L.x_perm), s));
 }
 
 moe_status_t moe_combine(const moe_config_t* cfg, const float* y_perm, const float* topk_w,
@@ -498,13 +511,11 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
                                  dmask, status, s, &lc));
   }
   MOE_TRY_CUDA(mark(MOE_STAGE_GATHER));
-  void* x_perm = at<char>(ws, L.x_perm);
-  MOE_TRY_CUDA(launch_gather(c, x, perm, offsets, x_perm, status, s, &lc));
   const bool has_shared = ws_gate != nullptr;
   ExpertArgs a{};
   a.x = x;
-  a.x_perm = x_perm;
   a.offsets = offsets;
+  a.perm = perm;
   a.w_gate = w_gate;
   a.w_up = w_up;
   a.w_down = w_down;
@@ -521,7 +532,7 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
   a.ev_up = ev ? ev[MOE_STAGE_GATE_UP] : nullptr;
   a.ev_down = ev ? ev[MOE_STAGE_DOWN] : nullptr;
   a.launches = &lc;
-  MOE_TRY_CUDA(run_experts(c, a, s));
+  MOE_TRY_CUDA(run_experts(c, a, at<char>(ws, L.x_perm), s));
   MOE_TRY_CUDA(mark(MOE_STAGE_COMBINE));
   if (ec)
     MOE_TRY_CUDA(launch_ec_combine(c, a.y_perm, at<int32_t>(ws, L.ec_rowmap), ec_w, a.y_shared,
