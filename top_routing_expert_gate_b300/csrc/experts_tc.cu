@@ -29,6 +29,16 @@
 // For gate/up, the B tile's first 128 rows are W_gate rows and the next 128
 // the matching W_up rows, so one N=256 MMA produces both halves and the
 // SwiGLU pairs column j with column 128 + j of the same accumulator.
+//
+// A group's last token tile is usually partial (an expert of the
+// DeepSeek-V3-shaped layer holds ~256 rows, so about one tile in five
+// would be mostly padding), and a tokens-in-M MMA costs the same whatever
+// rows it holds.  A partial tile therefore runs transposed on the same
+// shared-memory stages: two MMAs per K step with the B tile's two 128-row
+// weight halves as M and the tile's tokens, rounded up to 16, as N, into
+// columns 0.. and 128.. of the accumulator.  Each TMEM lane then holds one
+// weight row (gate and up of the same feature in one thread, so the SwiGLU
+// still needs no exchange), and the MMA time follows the tile's rows.
 #include "tc_common.cuh"
 
 #include <cudaTypedefs.h>
@@ -260,6 +270,10 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        // a partial token tile runs transposed: weight rows in M, its tokens in N
+        const int valid = min(BM, s_rows[g] - m * BM);
+        const bool part = valid < BM;
+        const uint32_t idesc_t = idesc_bf16_f32(BM, (uint32_t)((valid + 15) & ~15));
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
             failed = true;
@@ -268,11 +282,25 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
           tc_fence_after();
           const uint64_t a_desc = sdesc_k128(sA + stage * A_STAGE);
           const uint64_t b_desc = sdesc_k128(sB + stage * B_STAGE);
+          if (!part) {
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            // advance 16 bf16 = 32 bytes along K inside the swizzle span
-            mma_bf16(d_tmem, a_desc + (uint64_t)(2 * kk), b_desc + (uint64_t)(2 * kk), idesc,
-                     (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              // advance 16 bf16 = 32 bytes along K inside the swizzle span
+              mma_bf16(d_tmem, a_desc + (uint64_t)(2 * kk), b_desc + (uint64_t)(2 * kk), idesc,
+                       (kb | kk) != 0 ? 1u : 0u);
+            }
+          } else {
+            // D[w, t] for the B tile's two 128-row halves (gate and up
+            // weights, or two blocks of 128 down-projection outputs) into
+            // columns 0.. and 128.. of the buffer; N = the tokens rounded to 16
+            const uint64_t b_desc1 = sdesc_k128(sB + stage * B_STAGE + B_STAGE / 2);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              mma_bf16(d_tmem, b_desc + (uint64_t)(2 * kk), a_desc + (uint64_t)(2 * kk), idesc_t,
+                       (kb | kk) != 0 ? 1u : 0u);
+              mma_bf16(d_tmem + 128u, b_desc1 + (uint64_t)(2 * kk), a_desc + (uint64_t)(2 * kk),
+                       idesc_t, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           mma_commit(empty_bar(stage));
           if (++stage == STAGES) {
@@ -387,12 +415,60 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
         break;
       }
       tc_fence_after();
+      const int valid = min(BM, s_rows[g] - m * BM);   // token rows of the tile
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      if (valid < BM) {
+        // Transposed (partial) tile: this thread's TMEM lane is weight row
+        // w = 32q + lane of each 128-row half, one column per token.  For a
+        // token, the warp's 32 lanes store 32 consecutive outputs.
+        const int w = q * 32 + lane;
+        const size_t row0 = (size_t)(kind ? 0 : s_row0[g]) + (size_t)(m * BM);
+        if (MODE == kGateUp) {
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out[kind]) +
+                               row0 * p.ld_out[kind] + (size_t)n * 128 + (size_t)w;
+#pragma unroll 1
+          for (int c0 = 0; c0 < valid; c0 += 16) {
+            uint32_t gv[16], uv[16];
+            tmem_ld_32x32b_x16(tbase + (uint32_t)c0, gv);
+            tmem_ld_32x32b_x16(tbase + 128u + (uint32_t)c0, uv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (c0 + i < valid)
+                out[(size_t)(c0 + i) * p.ld_out[kind]] =
+                    __float2bfloat16_rn(silu_f(bits_f(gv[i])) * bits_f(uv[i]));
+          }
+        } else {
+          const int ncols = p.N[kind] - n * BN;   // outputs of this n tile
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            if (half * 128 >= ncols) break;
+            const bool fvalid = half * 128 + w < ncols;
+            float* out = reinterpret_cast<float*>(p.out[kind]) + row0 * p.ld_out[kind] +
+                         (size_t)n * BN + (size_t)(half * 128 + w);
+#pragma unroll 1
+            for (int c0 = 0; c0 < valid; c0 += 16) {
+              uint32_t v[16];
+              tmem_ld_32x32b_x16(tbase + (uint32_t)(half * 128 + c0), v);
+              tmem_ld_wait();
+              if (fvalid) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  if (c0 + i < valid) out[(size_t)(c0 + i) * p.ld_out[kind]] = bits_f(v[i]);
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce_bar(buf));
+        continue;
+      }
       // Each thread holds one row of the tile (TMEM lane) for 32 columns per
       // load.  The warp passes its 32 x 32 block through shared memory so
       // that every global store writes contiguous bytes of one or two rows.
       const int rows_left = s_rows[g] - (m * BM + q * 32);   // valid rows of this warp's block
       const size_t row_base = (size_t)(kind ? 0 : s_row0[g]) + (size_t)(m * BM + q * 32);
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
       uint32_t* st = epi_stage + q * kStageWords;
       if (MODE == kGateUp) {
         uint32_t* out = reinterpret_cast<uint32_t*>(p.out[kind]);   // bf16 pairs
