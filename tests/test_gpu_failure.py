@@ -51,19 +51,11 @@ def test_selftest_rejects_bad_limits():
     assert lib.moe_selftest_bounded_wait(None, 0, 1000, None) == B.MOE_ERR_WORKSPACE
 
 
-@pytest.mark.parametrize("gather", ["fused", "kernel"])
-def test_out_of_range_permutation_is_reported_not_read(gather, monkeypatch):
+def test_out_of_range_permutation_is_reported_not_read():
     # moe_grouped_swiglu takes the caller's permutation.  A grouped row naming
     # an assignment past the batch is recorded in the status word
-    # (MOE_ERR_DEVICE) and nothing outside x is read, by the gate/up kernel's
-    # own gather warp (it reads row 0 instead) and by the separate gather
-    # kernel (it skips the row) alike; the next call on the same workspace is
-    # clean.
-    if gather == "kernel":
-        monkeypatch.setenv("MOE_B300_SEPARATE_GATHER", "1")
-    else:
-        monkeypatch.delenv("MOE_B300_SEPARATE_GATHER", raising=False)
-    monkeypatch.setenv("MOE_B300_EXPERT_LAYOUT", "tokens_m")
+    # (MOE_ERR_DEVICE) and the gather skips it, reading nothing outside x; the
+    # next call on the same workspace is clean.
     s = MoEShape("bad_perm", T=96, d=128, E=4, k=2, F=128, F_s=0, gate="softmax",
                  renormalize=True, rsf=1.0, capacity_factor=None, zipf_s=None, dtype="bf16")
     cfg = moe.config_from_shape(s)

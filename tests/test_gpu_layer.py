@@ -86,18 +86,13 @@ def _layer_and_routing(s, inp, ws=None):
     return cfg, out, lib
 
 
-# the bf16 grouped GEMMs: tokens in the MMA's M with the gather fused into
-# the gate/up kernel (default), the same with the separate gather kernel, and
-# the expert weights in M on CTA pairs
-LAYOUTS = ["tokens_m", "tokens_m_gather_kernel", "weights_m"]
+# the bf16 grouped GEMMs: tokens in the MMA's M (default; a partial token
+# tile runs transposed), and the expert weights in M on CTA pairs
+LAYOUTS = ["tokens_m", "weights_m"]
 
 
 def _set_layout(monkeypatch, layout):
-    monkeypatch.setenv("MOE_B300_EXPERT_LAYOUT", layout.replace("_gather_kernel", ""))
-    if layout.endswith("_gather_kernel"):
-        monkeypatch.setenv("MOE_B300_SEPARATE_GATHER", "1")
-    else:
-        monkeypatch.delenv("MOE_B300_SEPARATE_GATHER", raising=False)
+    monkeypatch.setenv("MOE_B300_EXPERT_LAYOUT", layout)
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)

@@ -142,6 +142,8 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, int A, int E, int capac
 }
 
 // One warp per grouped row, 16-byte vectors; row r holds token perm[r] / k.
+// Each lane keeps eight 16-byte loads in flight before storing them, so a
+// warp moves 4 KB of a row per round trip to memory.
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
                    const int32_t* __restrict__ offsets, int E, int k, int T, int rows_cap,
@@ -162,7 +164,15 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm
     }
     const uint4* src = x + (size_t)t * row_vec;
     uint4* dst = x_perm + (size_t)r * row_vec;
-    for (int v = lane; v < row_vec; v += 32) dst[v] = __ldg(src + v);
+    for (int v0 = lane; v0 < row_vec; v0 += 32 * 8) {
+      uint4 buf[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (v0 + 32 * i < row_vec) buf[i] = __ldg(src + v0 + 32 * i);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (v0 + 32 * i < row_vec) dst[v0 + 32 * i] = buf[i];
+    }
   }
 }
 

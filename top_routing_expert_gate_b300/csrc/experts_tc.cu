@@ -12,7 +12,7 @@
 // The tile list is derived on the device from `offsets`, so no host
 // synchronisation separates dispatch from the GEMMs.
 //
-// Kernel structure (one persistent CTA per SM, 224 threads):
+// Kernel structure (one persistent CTA per SM, 192 threads):
 //   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per k-block
 //               (128-byte swizzle) into a 4-stage shared-memory ring;
 //   warp 1      allocates 512 TMEM columns; one thread issues
@@ -20,12 +20,7 @@
 //               accumulators and commits stage / accumulator barriers;
 //   warps 2..5  epilogue: tcgen05.ld of its 32 TMEM lanes, SwiGLU (gate/up)
 //               or plain fp32 (down), transposed through shared memory so
-//               that each global store writes whole row segments;
-//   warp 6      gate/up with the gather fused: loads the A tile itself, each
-//               row straight from the token's row of x (token = perm[row] / k
-//               for a routed expert, the row itself for the shared expert),
-//               with 16-byte cp.async into the 128-byte-swizzled layout the
-//               TMA would write, so the grouped copy of x is never built.
+//               that each global store writes whole row segments.
 // For gate/up, the B tile's first 128 rows are W_gate rows and the next 128
 // the matching W_up rows, so one N=256 MMA produces both halves and the
 // SwiGLU pairs column j with column 128 + j of the same accumulator.
@@ -57,12 +52,10 @@ constexpr int STAGES = 4;
 constexpr uint32_t A_STAGE = BM * BK * 2;   // 16 KB
 constexpr uint32_t B_STAGE = BN * BK * 2;   // 32 KB
 constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE;
-constexpr int kThreads = 224;        // grouped GEMM: 7 warps
-constexpr int kRouterThreads = 192;  // router GEMM: 6 warps
-constexpr int kGatherLag = 2;        // k-blocks the gather warp keeps in flight before signalling
+constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxGroups = kMaxExperts + 1;
-constexpr uint32_t kCtrlBytes = 256 + 4 * (kMaxGroups + 1 + 3 * kMaxGroups) + 4 * BM;
+constexpr uint32_t kCtrlBytes = 256 + 4 * (kMaxGroups + 1 + 3 * kMaxGroups);
 // Epilogue staging: per epilogue warp, 32 rows x 33 words (one word of
 // padding keeps both the row-wise writes and the column-wise reads free of
 // bank conflicts).
@@ -86,13 +79,6 @@ struct TcParams {
   int has_shared;
   int32_t* status;
   uint64_t timeout_ns;
-  // gate/up with the gather fused (gather != 0): A rows come from x, row r of
-  // routed group g being token perm[offsets[g] + r] / gather_div
-  int gather;
-  const uint8_t* gx;        // x [T, d] act
-  size_t gx_row_bytes;      // d * 2
-  const int32_t* perm;
-  int gather_div;
 };
 
 __device__ __forceinline__ int n_tiles_of(int mode, int N) {
@@ -123,11 +109,9 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
   int* s_row0 = s_tile_start + (kMaxGroups + 1);
   int* s_rows = s_row0 + kMaxGroups;
   int* s_mtiles = s_rows + kMaxGroups;
-  int* s_tok = s_mtiles + kMaxGroups;   // [BM] token rows of the gather warp's tile
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.E + (p.has_shared ? 1 : 0);
-  const bool gather = MODE == kGateUp && p.gather != 0;
   const int nt_r = n_tiles_of(MODE, p.N[0]);
   const int nt_s = n_tiles_of(MODE, p.N[1]);
 
@@ -147,9 +131,7 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      // with the gather fused a stage is full once the producer's weight
-      // bytes have landed and the gather warp has signalled its A rows
-      mbar_init(full_bar(s), gather ? 2 : 1);
+      mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -161,7 +143,7 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    if (!gather) prefetch_tensormap(&p.a_map[0]);
+    prefetch_tensormap(&p.a_map[0]);
     prefetch_tensormap(&p.b_map[0]);
     if (MODE == kGateUp) prefetch_tensormap(&p.u_map[0]);
   }
@@ -220,10 +202,10 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
             break;
           }
           const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, gather ? B_STAGE : STAGE_TX);
+          mbar_arrive_expect_tx(fb, STAGE_TX);
           const uint32_t a_dst = sA + stage * A_STAGE;
           const uint32_t b_dst = sB + stage * B_STAGE;
-          if (!gather) tma_load_2d(a_dst, &p.a_map[kind], fb, kb * BK, a_row);
+          tma_load_2d(a_dst, &p.a_map[kind], fb, kb * BK, a_row);
           if (MODE == kGateUp) {
             tma_load_2d(b_dst, &p.b_map[kind], fb, kb * BK, b_row);
             tma_load_2d(b_dst + B_STAGE / 2, &p.u_map[kind], fb, kb * BK, b_row);
@@ -317,87 +299,6 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
         // let every MMA already issued finish before the CTA tears down
         mma_commit(drain_bar);
         mbar_wait(drain_bar, 0, nullptr, p.timeout_ns);
-      }
-    }
-  } else if (warp == 6) {
-    if (gather) {
-      // ---------------- gather warp: A rows straight from x ----------------
-      // Per k-block this lane copies 16-byte chunk (lane & 7) of rows
-      // 4j + (lane >> 3), j = 0..31, so each warp instruction reads four
-      // whole 128-byte row segments.  Chunk c of row r goes to chunk
-      // c ^ (r & 7) of the row (the 128-byte swizzle).  Rows past the tile's
-      // valid rows are not loaded: their MMA rows are discarded.  A k-block
-      // is signalled full kGatherLag k-blocks after it was issued, once this
-      // thread's copies of it are complete and fenced for the tensor core.
-      int stage = 0, issued = 0;
-      uint32_t phase = 0;
-      const int chunk = lane & 7;
-      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
-        int g, m, n;
-        decode(t, g, m, n);
-        const int kind = g < p.E ? 0 : 1;
-        const int nk = p.K[kind] / BK;
-        const int valid = min(BM, s_rows[g] - m * BM);
-#pragma unroll
-        for (int i = 0; i < BM / 32; ++i) {
-          const int r = lane + 32 * i;
-          int tok = 0;
-          if (r < valid) {
-            tok = m * BM + r;
-            if (kind == 0) {
-              const int a = __ldg(p.perm + s_row0[g] + tok);
-              tok = a / p.gather_div;
-              if (a < 0 || tok >= p.T) {   // a row outside x: record it, read row 0
-                record_error(p.status, kDevBadIndex);
-                tok = 0;
-              }
-            }
-          }
-          s_tok[r] = tok;
-        }
-        __syncwarp();
-        int tokr[BM / 4];
-#pragma unroll
-        for (int j = 0; j < BM / 4; ++j) tokr[j] = s_tok[4 * j + (lane >> 3)];
-        __syncwarp();
-        for (int kb = 0; kb < nk; ++kb) {
-          const bool ok = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns);
-          if (!__all_sync(0xffffffffu, ok)) {
-            failed = true;
-            break;
-          }
-          const uint32_t a_dst = sA + stage * A_STAGE;
-          const uint8_t* src0 = p.gx + (size_t)kb * (BK * 2) + (size_t)chunk * 16;
-#pragma unroll
-          for (int j = 0; j < BM / 4; ++j) {
-            const int r = 4 * j + (lane >> 3);
-            if (r < valid)
-              cp_async16(a_dst + (uint32_t)r * 128u + ((uint32_t)(chunk ^ (r & 7)) << 4),
-                         src0 + (size_t)tokr[j] * p.gx_row_bytes);
-          }
-          cp_async_commit();
-          if (issued >= kGatherLag) {
-            cp_async_wait<kGatherLag>();
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(full_bar((issued - kGatherLag) % STAGES));
-          }
-          ++issued;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      // signal the k-blocks still owed (never leave with copies in flight)
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0)
-        for (int i = max(0, issued - kGatherLag); i < issued; ++i) mbar_arrive(full_bar(i % STAGES));
-      if (failed) {
-        *abort_flag = 1;
-        if (lane == 0) record_error(p.status, kDevTimeout);
       }
     }
   } else {
@@ -555,7 +456,7 @@ struct RouterParams {
 
 constexpr uint32_t kRouterSmemMax = STAGES * (A_STAGE + B_STAGE) + 256 + 1024;
 
-__global__ void __launch_bounds__(kRouterThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 router_gemm_kernel(const __grid_constant__ RouterParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -753,7 +654,7 @@ cudaError_t launch_router_tc(const moe_config_t& c, const void* x, const void* w
   });
   if (attr_err != cudaSuccess) return attr_err;
   const uint32_t smem = STAGES * (A_STAGE + (uint32_t)p.E_pad * 128u) + 256 + 1024;
-  router_gemm_kernel<<<plan.m_tiles * plan.splits, kRouterThreads, smem, s>>>(p);
+  router_gemm_kernel<<<plan.m_tiles * plan.splits, kThreads, smem, s>>>(p);
   count_launch(lc);
   return cudaGetLastError();
 }
@@ -767,17 +668,8 @@ cudaError_t launch_gemm_tc(const moe_config_t& c, const ExpertArgs& a, int which
 
   TcParams p1{};
   bool ok = true;
-  if (a.gather_div > 0) {
-    // the gather is fused: the A rows are read from x by the gather warp
-    p1.gather = 1;
-    p1.gx = static_cast<const uint8_t*>(a.x);
-    p1.gx_row_bytes = (size_t)d * 2;
-    p1.perm = a.perm;
-    p1.gather_div = a.gather_div;
-  } else {
-    ok &= make_map(&p1.a_map[0], a.x_perm, d, A, BM);
-    ok &= make_map(&p1.a_map[1], a.x, d, T, BM);
-  }
+  ok &= make_map(&p1.a_map[0], a.x_perm, d, A, BM);
+  ok &= make_map(&p1.a_map[1], a.x, d, T, BM);
   ok &= make_map(&p1.b_map[0], a.w_gate, d, (uint64_t)E * F, 128);
   ok &= make_map(&p1.u_map[0], a.w_up, d, (uint64_t)E * F, 128);
   if (has_shared) {
@@ -806,7 +698,6 @@ cudaError_t launch_gemm_tc(const moe_config_t& c, const ExpertArgs& a, int which
   p1.timeout_ns = kWaitTimeoutNs;
 
   TcParams p2 = p1;
-  p2.gather = 0;
   ok = true;
   ok &= make_map(&p2.a_map[0], a.h, F, A, BM);
   ok &= make_map(&p2.b_map[0], a.w_down, F, (uint64_t)E * d, BN);

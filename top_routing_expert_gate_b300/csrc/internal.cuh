@@ -192,12 +192,9 @@ cudaError_t launch_combine(const moe_config_t& c, const float* y_perm, const flo
 // x_perm / h; the shared group (when ws_* given) takes all T rows of x / h_shared.
 struct ExpertArgs {
   const void* x;        // [T, d]
-  const void* x_perm;   // [A, d], built by the gather unless the GEMM fuses it
+  const void* x_perm;   // [A, d], built by the gather in run_experts
   const int32_t* offsets;
   const int32_t* perm = nullptr;   // grouped row -> assignment (token choice) or token
-  // > 0: the gate/up GEMM reads its A rows from x itself, row r of the
-  // routed groups being token perm[r] / gather_div (no x_perm)
-  int gather_div = 0;
   const void* w_gate; const void* w_up; const void* w_down;
   const void* ws_gate; const void* ws_up; const void* ws_down;
   void* h;              // [A, F]

@@ -167,19 +167,12 @@ int fp8_tmem_tile(const moe_config_t& c) {
   return (int64_t)c.T * c.top_k <= (int64_t)64 * c.n_experts && c.T <= 256 ? 64 : 128;
 }
 
-// The gather (x_perm[r] = x[perm[r] / div]) and the two grouped GEMMs.  The
-// bf16 tokens-in-M gate/up kernel reads its A rows from x itself, so for it
-// no gather runs and no x_perm is written.
+// The gather (x_perm[r] = x[perm[r] / div]) and the two grouped GEMMs.
 cudaError_t run_experts(const moe_config_t& c, ExpertArgs a, void* x_perm, cudaStream_t s) {
   const bool fp8 = c.weight_format == MOE_WEIGHTS_FP8_E4M3;
   const int fp8_tn = fp8 ? fp8_tmem_tile(c) : 0;
   const int div = c.routing == MOE_ROUTE_EXPERT_CHOICE ? 1 : c.top_k;
-  const bool fused_gather =
-      c.act_dtype == MOE_BF16 && !fp8 && !weights_in_m(c, kGemmGateUp) &&
-      getenv("MOE_B300_SEPARATE_GATHER") == nullptr;
-  if (fused_gather) {
-    a.gather_div = div;
-  } else {
+  {
     const cudaError_t e = launch_gather(c, a.x, a.perm, a.offsets, x_perm, a.status, s,
                                         a.launches, div);
     if (e != cudaSuccess) return e;

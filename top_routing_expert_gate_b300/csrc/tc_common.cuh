@@ -87,26 +87,6 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// ---- per-thread 16-byte asynchronous copies (cp.async) ----
-
-// 16 bytes global -> shared, cached in L2 only.  Both addresses 16-byte aligned.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-// Waits until at most N of this thread's committed groups are still pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-// Orders this thread's completed shared-memory writes (generic proxy) before
-// later reads of the same memory by the async proxy (tcgen05.mma operands).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ---- CTA pairs (clusters of two CTAs sharing one tcgen05 MMA) ----
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
