@@ -54,7 +54,6 @@ constexpr uint32_t B_STAGE = BN * BK * 2;   // 32 KB
 constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr int TQ = 4;              // tile-index queue slots (producer -> MMA, epilogue)
 constexpr int kMaxGroups = kMaxExperts + 1;
 constexpr uint32_t kCtrlBytes = 256 + 4 * (kMaxGroups + 1 + 3 * kMaxGroups);
 // Epilogue staging: per epilogue warp, 32 rows x 33 words (one word of
@@ -80,7 +79,6 @@ struct TcParams {
   int has_shared;
   int32_t* status;
   uint64_t timeout_ns;
-  int* tile_counter;      // next tile to hand out; zero at launch
 };
 
 __device__ __forceinline__ int n_tiles_of(int mode, int N) {
@@ -99,20 +97,14 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
   uint32_t* epi_stage = reinterpret_cast<uint32_t*>(smem + STAGES * (A_STAGE + B_STAGE));
   uint8_t* ctrl = smem + STAGES * (A_STAGE + B_STAGE) + kEpiBytes;
   const uint32_t bar0 = smem_u32(ctrl);
-  // barriers: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain,
-  // tile-queue full[TQ], tile-queue empty[TQ]
+  // barriers: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
   auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
   auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  auto tqf_bar = [&](int j) { return bar0 + 8u * (2 * STAGES + 5 + j); };
-  auto tqe_bar = [&](int j) { return bar0 + 8u * (2 * STAGES + 5 + TQ + j); };
-  constexpr int kBars = 2 * STAGES + 5 + 2 * TQ;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * kBars);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 8 * kBars + 4);
-  volatile int* s_tq = reinterpret_cast<volatile int*>(ctrl + 8 * kBars + 8);   // [TQ]
-  static_assert(8 * kBars + 8 + 4 * TQ <= 256, "control block");
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * STAGES + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 8 * (2 * STAGES + 5) + 4);
   int* s_tile_start = reinterpret_cast<int*>(ctrl + 256);
   int* s_row0 = s_tile_start + (kMaxGroups + 1);
   int* s_rows = s_row0 + kMaxGroups;
@@ -147,10 +139,6 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
       mbar_init(acce_bar(b), 4);
     }
     mbar_init(drain_bar, 1);
-    for (int j = 0; j < TQ; ++j) {
-      mbar_init(tqf_bar(j), 1);   // the producer publishes a tile index
-      mbar_init(tqe_bar(j), 5);   // the MMA thread and the four epilogue warps read it
-    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -178,11 +166,6 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
   const uint32_t tmem_base = *tmem_slot;
   const int total = s_tile_start[G];
 
-  // Tiles are handed out in order from a global counter, each to the CTA
-  // that asks first, so CTAs that drew cheap (partial) tiles take more of
-  // them.  The producer takes the index and passes it to the MMA thread and
-  // the epilogue through a TQ-slot queue in shared memory (-1: no more).
-  //
   // tile t -> (group, m tile, n tile); m varies fastest so CTAs running at
   // the same time share the weight tile (L2 reuse of the B operand).
   auto decode = [&](int t, int& g, int& m, int& n) {
@@ -206,23 +189,7 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
-      int qs = 0;
-      uint32_t qphase = 0;
-      int next = atomicAdd(p.tile_counter, 1);
-      while (!failed) {
-        const int t = next < total ? next : -1;
-        if (!mbar_wait(tqe_bar(qs), qphase ^ 1u, abort_flag, p.timeout_ns)) {
-          failed = true;
-          break;
-        }
-        s_tq[qs] = t;
-        mbar_arrive(tqf_bar(qs));
-        if (++qs == TQ) {
-          qs = 0;
-          qphase ^= 1u;
-        }
-        if (t < 0) break;
-        next = atomicAdd(p.tile_counter, 1);   // in flight while this tile loads
+      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
         int g, m, n;
         decode(t, g, m, n);
         const int kind = g < p.E ? 0 : 1;
@@ -271,20 +238,8 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
       int stage = 0;
       uint32_t phase = 0;
-      int qs = 0;
-      uint32_t qphase = 0;
-      for (int local = 0; !failed; ++local) {
-        if (!mbar_wait(tqf_bar(qs), qphase, abort_flag, p.timeout_ns)) {
-          failed = true;
-          break;
-        }
-        const int t = s_tq[qs];
-        mbar_arrive(tqe_bar(qs));
-        if (++qs == TQ) {
-          qs = 0;
-          qphase ^= 1u;
-        }
-        if (t < 0) break;
+      int local = 0;
+      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x, ++local) {
         int g, m, n;
         decode(t, g, m, n);
         const int kind = g < p.E ? 0 : 1;
@@ -349,21 +304,8 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     const int q = warp & 3;   // TMEM lane quarter this warp may access
-    int qs = 0;
-    uint32_t qphase = 0;
-    for (int local = 0;; ++local) {
-      if (!__all_sync(0xffffffffu, mbar_wait(tqf_bar(qs), qphase, abort_flag, p.timeout_ns))) {
-        failed = true;
-        break;
-      }
-      const int t = s_tq[qs];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tqe_bar(qs));
-      if (++qs == TQ) {
-        qs = 0;
-        qphase ^= 1u;
-      }
-      if (t < 0) break;
+    int local = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
       int g, m, n;
       decode(t, g, m, n);
       const int kind = g < p.E ? 0 : 1;
@@ -664,9 +606,6 @@ cudaError_t launch(const TcParams& p, cudaStream_t s) {
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  // the kernel hands tiles out from this counter, which must start at zero
-  const cudaError_t e = cudaMemsetAsync(p.tile_counter, 0, sizeof(int), s);
-  if (e != cudaSuccess) return e;
   grouped_gemm_kernel<MODE><<<num_sms(), kThreads, kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
@@ -757,11 +696,8 @@ cudaError_t launch_gemm_tc(const moe_config_t& c, const ExpertArgs& a, int which
   p1.has_shared = has_shared ? 1 : 0;
   p1.status = a.status;
   p1.timeout_ns = kWaitTimeoutNs;
-  p1.tile_counter = a.tile_counter;
-  if (!p1.tile_counter) return cudaErrorInvalidValue;
 
   TcParams p2 = p1;
-  p2.tile_counter = a.tile_counter + 1;
   ok = true;
   ok &= make_map(&p2.a_map[0], a.h, F, A, BM);
   ok &= make_map(&p2.b_map[0], a.w_down, F, (uint64_t)E * d, BN);

@@ -54,7 +54,6 @@ struct WsLayout {
   size_t ec_scores;   // [E, T] fp32 (expert choice)
   size_t ec_w;        // [E, C] fp32 (expert choice)
   size_t ec_rowmap;   // [T, E] int32 (expert choice)
-  size_t sched;       // int32 tile counters of the grouped GEMMs (zeroed before each launch)
   size_t total;
   int nb;             // dispatch blocks
 };
@@ -196,7 +195,6 @@ struct ExpertArgs {
   const void* x_perm;   // [A, d], built by the gather in run_experts
   const int32_t* offsets;
   const int32_t* perm = nullptr;   // grouped row -> assignment (token choice) or token
-  int* tile_counter = nullptr;     // [2] workspace counters of the tokens-in-M GEMMs
   const void* w_gate; const void* w_up; const void* w_down;
   const void* ws_gate; const void* ws_up; const void* ws_down;
   void* h;              // [A, F]

@@ -48,7 +48,6 @@ WsLayout ws_layout(const moe_config_t& c) {
   L.ec_scores = take(ec ? E * T * 4 : 0);
   L.ec_w = take(ec ? R * 4 : 0);
   L.ec_rowmap = take(ec ? T * E * 4 : 0);
-  L.sched = take(64);
   L.total = o;
   return L;
 }
@@ -384,7 +383,6 @@ moe_status_t moe_grouped_swiglu(const moe_config_t* cfg, const void* x, const in
   a.status = status;
   a.scales = scales;
   a.rows = (int)grouped_rows(*cfg);
-  a.tile_counter = at<int>(ws, L.sched);
   return cuda_status(run_experts(*cfg, a, at<char>(ws, L.x_perm), s));
 }
 
@@ -527,7 +525,6 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
   a.ev_up = ev ? ev[MOE_STAGE_GATE_UP] : nullptr;
   a.ev_down = ev ? ev[MOE_STAGE_DOWN] : nullptr;
   a.launches = &lc;
-  a.tile_counter = at<int>(ws, L.sched);
   MOE_TRY_CUDA(run_experts(c, a, at<char>(ws, L.x_perm), s));
   MOE_TRY_CUDA(mark(MOE_STAGE_COMBINE));
   if (ec)
