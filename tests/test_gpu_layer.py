@@ -87,12 +87,17 @@ def _layer_and_routing(s, inp, ws=None):
 
 
 # the bf16 grouped GEMMs: tokens in the MMA's M (default; a partial token
-# tile runs transposed), and the expert weights in M on CTA pairs
-LAYOUTS = ["tokens_m", "weights_m"]
+# tile runs transposed), the same with partial tiles run like full ones, and
+# the expert weights in M on CTA pairs
+LAYOUTS = ["tokens_m", "tokens_m_full_tail", "weights_m"]
 
 
 def _set_layout(monkeypatch, layout):
-    monkeypatch.setenv("MOE_B300_EXPERT_LAYOUT", layout)
+    monkeypatch.setenv("MOE_B300_EXPERT_LAYOUT", layout.replace("_full_tail", ""))
+    if layout.endswith("_full_tail"):
+        monkeypatch.setenv("MOE_B300_PARTIAL_TILE", "full")
+    else:
+        monkeypatch.delenv("MOE_B300_PARTIAL_TILE", raising=False)
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)

@@ -39,6 +39,8 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <stdlib.h>
+#include <string.h>
 
 namespace moe {
 namespace {
@@ -79,6 +81,7 @@ struct TcParams {
   int has_shared;
   int32_t* status;
   uint64_t timeout_ns;
+  int transpose_partial;  // run a partial token tile transposed (weights in M)
 };
 
 __device__ __forceinline__ int n_tiles_of(int mode, int N) {
@@ -254,7 +257,7 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
         // a partial token tile runs transposed: weight rows in M, its tokens in N
         const int valid = min(BM, s_rows[g] - m * BM);
-        const bool part = valid < BM;
+        const bool part = valid < BM && p.transpose_partial;
         const uint32_t idesc_t = idesc_bf16_f32(BM, (uint32_t)((valid + 15) & ~15));
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
@@ -318,7 +321,7 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
       tc_fence_after();
       const int valid = min(BM, s_rows[g] - m * BM);   // token rows of the tile
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-      if (valid < BM) {
+      if (valid < BM && p.transpose_partial) {
         // Transposed (partial) tile: this thread's TMEM lane is weight row
         // w = 32q + lane of each 128-row half, one column per token.  For a
         // token, the warp's 32 lanes store 32 consecutive outputs.
@@ -696,6 +699,10 @@ cudaError_t launch_gemm_tc(const moe_config_t& c, const ExpertArgs& a, int which
   p1.has_shared = has_shared ? 1 : 0;
   p1.status = a.status;
   p1.timeout_ns = kWaitTimeoutNs;
+  // a partial token tile runs transposed unless MOE_B300_PARTIAL_TILE=full
+  // (a tuning and test override)
+  const char* pt = getenv("MOE_B300_PARTIAL_TILE");
+  p1.transpose_partial = pt && strcmp(pt, "full") == 0 ? 0 : 1;
 
   TcParams p2 = p1;
   ok = true;
