@@ -202,40 +202,7 @@ def test_empty_batch():
     assert out["counts"].sum().item() == 0 and out["mean_prob"].abs().sum().item() == 0
 
 
-def _assert_fused_matches_split(y_fused, y_split, y_perm, y_sh, gate_w, topk_w, dsp, T, k,
-                                layout):
-    """The fused call against the split entry points on the same inputs.
-    With fp32 down-projection rows in both (weights in M) the two are the
-    same arithmetic and must agree bit for bit.  With tokens in M the fused
-    call stores those rows as fp16 times a power of two per 32 columns: each
-    term g * Y then differs by at most 2^-11 of itself, and the fp32 sums by
-    a few ulp of the sum of magnitudes."""
-    if layout == "weights_m":
-        assert torch.equal(y_fused, y_split)
-        return
-    A = T * k
-    n = int(dsp["offsets"][-1].item())
-    row_of = np.full(A, -1, dtype=np.int64)
-    row_of[np_i(dsp["perm"])[:n]] = np.arange(n)
-    Y = np_f(y_perm)
-    g = np_f(topk_w)
-    mag = np.zeros((T, Y.shape[1]))
-    for t in range(T):
-        for j in range(k):
-            r = row_of[t * k + j]
-            if r >= 0:
-                mag[t] += abs(g[t, j]) * np.abs(Y[r])
-    if y_sh is not None:
-        ws_ = np.ones(T) if gate_w is None else np_f(gate_w)
-        mag += np.abs(ws_)[:, None] * np.abs(np_f(y_sh))
-    bound = (2.0 ** -11 + 16 * 2.0 ** -24) * mag
-    diff = np.abs(np_f(y_fused) - np_f(y_split))
-    assert np.all(diff <= bound), float((diff - bound).max())
-
-
-@pytest.mark.parametrize("layout", ["tokens_m", "weights_m"])
-def test_deterministic_and_split_calls_match_fused(layout, monkeypatch):
-    _set_layout(monkeypatch, layout)
+def test_deterministic_and_split_calls_match_fused():
     s = MID_SHAPES["mid_sigmoid_shared"]
     inp = make_inputs(s, device=DEV, seed=6)
     cfg = moe.config_from_shape(s)
@@ -259,8 +226,7 @@ def test_deterministic_and_split_calls_match_fused(layout, monkeypatch):
                     y_sh, None, y, ws)
     torch.cuda.synchronize()
     assert torch.equal(r["topk_idx"], a["topk_idx"])
-    _assert_fused_matches_split(a["y"], y, y_perm, y_sh, None, r["topk_w"], dsp, s.T, s.k,
-                                layout)
+    assert torch.equal(y, a["y"])
     assert moe.moe_get_error(ws) == 0
 
 
@@ -299,9 +265,7 @@ def test_host_buffer_call_matches_device_call(out_dtype):
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("layout", ["tokens_m", "weights_m"])
-def test_gated_shared_expert_split_calls_match_fused(layout, monkeypatch):
-    _set_layout(monkeypatch, layout)
+def test_gated_shared_expert_split_calls_match_fused():
     s = MID_SHAPES["mid_gated_shared"]
     inp = make_inputs(s, device=DEV, seed=7)
     cfg = moe.config_from_shape(s)
@@ -321,8 +285,7 @@ def test_gated_shared_expert_split_calls_match_fused(layout, monkeypatch):
     moe.moe_combine(cfg, y_perm, r["topk_w"], dsp["offsets"], dsp["perm"], dsp["drop_mask"],
                     y_sh, gate_w, y, ws)
     torch.cuda.synchronize()
-    _assert_fused_matches_split(a["y"], y, y_perm, y_sh, gate_w, r["topk_w"], dsp, s.T, s.k,
-                                layout)
+    assert torch.equal(y, a["y"])
     # the gate weights themselves: sigmoid(x . w), fp32 accumulation of d bf16 products
     want = O.shared_gate_weights(to_f64(inp["x"]), to_f64(w.shared_gate))
     np.testing.assert_allclose(np_f(gate_w), want, rtol=0, atol=2e-6)

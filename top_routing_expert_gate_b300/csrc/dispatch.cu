@@ -16,8 +16,6 @@
 // lane rank), so every output is a pure function of topk_idx.
 #include "internal.cuh"
 
-#include <cuda_fp16.h>
-
 namespace moe {
 namespace {
 
@@ -265,82 +263,6 @@ combine_kernel(const float4* __restrict__ y_perm, const float* __restrict__ topk
   }
 }
 
-// The same combine over down-projection rows stored as fp16 with one
-// exponent byte per 32-column chunk (value = fp16 * 2^(byte - 127)):
-// y_exp[c * rows + r] for grouped row r, ys_exp[c * T + t] for the shared
-// expert.  Each decoded value is exact in fp32, and the sums run in the
-// same order as in combine_kernel.
-__device__ __forceinline__ float4 load_h4(const uint2* p, float sc) {
-  const uint2 u = __ldg(p);
-  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-  return make_float4(a.x * sc, a.y * sc, b.x * sc, b.y * sc);
-}
-__device__ __forceinline__ float exp_scale(const uint8_t* e) {
-  return __int_as_float((int)__ldg(e) << 23);
-}
-
-template <typename TOut>
-__global__ void __launch_bounds__(256)
-combine_h_kernel(const uint2* __restrict__ y_perm, const uint8_t* __restrict__ y_exp, int rows,
-                 const float* __restrict__ topk_w, const int32_t* __restrict__ row_of,
-                 const uint8_t* __restrict__ drop_mask, const uint2* __restrict__ y_shared,
-                 const uint8_t* __restrict__ ys_exp, const float* __restrict__ shared_w,
-                 TOut* __restrict__ y, int T, int k, int d, int A, int32_t* status) {
-  __shared__ int s_row[kMaxTopK];
-  __shared__ float s_g[kMaxTopK];
-  const int d4 = d >> 2;
-  for (int t = blockIdx.x; t < T; t += gridDim.x) {
-    if (threadIdx.x < k) {
-      const int a = t * k + threadIdx.x;
-      int r = -1;
-      if (!drop_mask[a]) {
-        r = row_of[a];
-        if (r < 0 || r >= A) {
-          record_error(status, kDevBadIndex);
-          r = -1;
-        }
-      }
-      s_row[threadIdx.x] = r;
-      s_g[threadIdx.x] = topk_w[a];
-    }
-    __syncthreads();
-    for (int v = threadIdx.x; v < d4; v += blockDim.x) {
-      const int chunk = v >> 3;   // 8 vectors of 4 columns per 32-column chunk
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int j = 0; j < k; ++j) {
-        const int r = s_row[j];
-        if (r < 0) continue;
-        const float g = s_g[j];
-        const float4 yv =
-            load_h4(y_perm + (size_t)r * d4 + v, exp_scale(y_exp + (size_t)chunk * rows + r));
-        acc.x = fmaf(g, yv.x, acc.x);
-        acc.y = fmaf(g, yv.y, acc.y);
-        acc.z = fmaf(g, yv.z, acc.z);
-        acc.w = fmaf(g, yv.w, acc.w);
-      }
-      if (y_shared) {
-        const float4 sv =
-            load_h4(y_shared + (size_t)t * d4 + v, exp_scale(ys_exp + (size_t)chunk * T + t));
-        if (shared_w) {
-          const float ws = __ldg(shared_w + t);
-          acc.x = fmaf(ws, sv.x, acc.x);
-          acc.y = fmaf(ws, sv.y, acc.y);
-          acc.z = fmaf(ws, sv.z, acc.z);
-          acc.w = fmaf(ws, sv.w, acc.w);
-        } else {
-          acc.x += sv.x;
-          acc.y += sv.y;
-          acc.z += sv.z;
-          acc.w += sv.w;
-        }
-      }
-      store4(y + (size_t)t * d + 4 * v, acc);
-    }
-    __syncthreads();
-  }
-}
-
 int sm_count() {
   static int n = 0;
   if (n == 0) {
@@ -405,28 +327,6 @@ cudaError_t launch_invert_perm(const moe_config_t& c, const int32_t* perm,
   int blocks = (A + 255) / 256;
   if (blocks > sm_count() * 4) blocks = sm_count() * 4;
   invert_perm_kernel<<<blocks, 256, 0, s>>>(perm, offsets, c.n_experts, A, row_of, status);
-  count_launch(lc);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_combine_h(const moe_config_t& c, const void* y_perm, const uint8_t* y_exp,
-                             int rows, const float* topk_w, const int32_t* row_of,
-                             const uint8_t* drop_mask, const void* y_shared,
-                             const uint8_t* ys_exp, const float* shared_w, void* y,
-                             int32_t* status, cudaStream_t s, LaunchCounter* lc) {
-  const int T = c.T;
-  if (T == 0) return cudaSuccess;
-  int blocks = T;
-  if (blocks > sm_count() * 16) blocks = sm_count() * 16;
-  const int A = T * c.top_k;
-  if (c.out_dtype == MOE_BF16)
-    combine_h_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
-        (const uint2*)y_perm, y_exp, rows, topk_w, row_of, drop_mask, (const uint2*)y_shared,
-        ys_exp, shared_w, (__nv_bfloat16*)y, T, c.top_k, c.d_model, A, status);
-  else
-    combine_h_kernel<float><<<blocks, 256, 0, s>>>(
-        (const uint2*)y_perm, y_exp, rows, topk_w, row_of, drop_mask, (const uint2*)y_shared,
-        ys_exp, shared_w, (float*)y, T, c.top_k, c.d_model, A, status);
   count_launch(lc);
   return cudaGetLastError();
 }

@@ -36,8 +36,6 @@
 // still needs no exchange), and the MMA time follows the tile's rows.
 #include "tc_common.cuh"
 
-#include <cuda_fp16.h>
-
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -84,22 +82,7 @@ struct TcParams {
   int32_t* status;
   uint64_t timeout_ns;
   int transpose_partial;  // run a partial token tile transposed (weights in M)
-  // down with oexp[kind] set: out[kind] holds fp16 rows, and oexp[kind][c * exp_rows[kind] + r]
-  // = 127 + s for row r's 32-column chunk c, whose values are fp16 * 2^s
-  uint8_t* oexp[2];
-  int exp_rows[2];
 };
-
-// Exponent s of a 32-value chunk stored in fp16: the largest magnitude m
-// (its fp32 bit pattern without the sign) scaled by 2^-s lands in
-// [2^14, 2^15), inside fp16's range with its full precision; s is kept in
-// [-126, 113] so that both 2^s and 2^-s are normal fp32 numbers.
-__device__ __forceinline__ int chunk_exponent(uint32_t max_abs_bits) {
-  if (max_abs_bits == 0) return 0;
-  const int e = (int)(max_abs_bits >> 23) - 127;   // floor(log2 m) for normal m
-  return min(max(e - 14, -126), 113);
-}
-__device__ __forceinline__ float pow2f(int s) { return __int_as_float((127 + s) << 23); }
 
 __device__ __forceinline__ int n_tiles_of(int mode, int N) {
   return mode == kGateUp ? N / 128 : (N + BN - 1) / BN;
@@ -361,35 +344,18 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
           }
         } else {
           const int ncols = p.N[kind] - n * BN;   // outputs of this n tile
-          uint8_t* oexp = p.oexp[kind];
 #pragma unroll 1
           for (int half = 0; half < 2; ++half) {
             if (half * 128 >= ncols) break;
             const bool fvalid = half * 128 + w < ncols;
-            const size_t col = (size_t)n * BN + (size_t)(half * 128 + w);
+            float* out = reinterpret_cast<float*>(p.out[kind]) + row0 * p.ld_out[kind] +
+                         (size_t)n * BN + (size_t)(half * 128 + w);
 #pragma unroll 1
             for (int c0 = 0; c0 < valid; c0 += 16) {
               uint32_t v[16];
               tmem_ld_32x32b_x16(tbase + (uint32_t)(half * 128 + c0), v);
               tmem_ld_wait();
-              if (oexp) {
-                // a token's 32-column chunk is this warp's 32 lanes
-                __half* out = reinterpret_cast<__half*>(p.out[kind]) + row0 * p.ld_out[kind] + col;
-                uint8_t* ex = oexp + ((size_t)n * BN + half * 128 + q * 32) / 32 *
-                                         (size_t)p.exp_rows[kind] + row0;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                  const int sx = chunk_exponent(
-                      __reduce_max_sync(0xffffffffu, fvalid ? (v[i] & 0x7fffffffu) : 0u));
-                  if (c0 + i < valid) {
-                    if (fvalid)
-                      out[(size_t)(c0 + i) * p.ld_out[kind]] =
-                          __float2half_rn(bits_f(v[i]) * pow2f(-sx));
-                    if (lane == 0) ex[c0 + i] = (uint8_t)(127 + sx);
-                  }
-                }
-              } else if (fvalid) {
-                float* out = reinterpret_cast<float*>(p.out[kind]) + row0 * p.ld_out[kind] + col;
+              if (fvalid) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                   if (c0 + i < valid) out[(size_t)(c0 + i) * p.ld_out[kind]] = bits_f(v[i]);
@@ -435,50 +401,23 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
           __syncwarp();
         }
       } else {
+        float* out = reinterpret_cast<float*>(p.out[kind]);
         const size_t ld = (size_t)p.ld_out[kind];
         const int ncols = p.N[kind] - n * BN;   // > 0, a multiple of 64
-        uint8_t* oexp = p.oexp[kind];
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           if (c >= ncols) break;
           uint32_t v[32];
           tmem_ld_32x32b_x32(tbase + (uint32_t)c, v);
           tmem_ld_wait();
-          if (oexp) {
-            // this thread's row: one 32-column chunk, stored as fp16 * 2^s
-            uint32_t mx = 0;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) mx = max(mx, v[j] & 0x7fffffffu);
-            const int sx = chunk_exponent(mx);
-            const float sc = pow2f(-sx);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              __half2 hv = __floats2half2_rn(bits_f(v[2 * j]) * sc, bits_f(v[2 * j + 1]) * sc);
-              st[lane * 33 + j] = *reinterpret_cast<uint32_t*>(&hv);
-            }
-            if (lane < rows_left)
-              oexp[((size_t)n * BN + c) / 32 * (size_t)p.exp_rows[kind] + row_base + lane] =
-                  (uint8_t)(127 + sx);
-            __syncwarp();
-            // two rows of 64 bytes per store: lanes 0..15 row r, lanes 16..31 row r + 1
-            uint32_t* out = reinterpret_cast<uint32_t*>(p.out[kind]);   // fp16 pairs
-            const size_t col2 = ((size_t)n * BN + (size_t)c) / 2 + (size_t)(lane & 15);
+          for (int j = 0; j < 32; ++j) st[lane * 33 + j] = v[j];
+          __syncwarp();
+          // one row of 128 bytes per store
+          const size_t col = (size_t)n * BN + (size_t)c + (size_t)lane;
 #pragma unroll 4
-            for (int r = 0; r < 32; r += 2) {
-              const int rr = r + (lane >> 4);
-              if (rr < rows_left) out[(row_base + rr) * (ld / 2) + col2] = st[rr * 33 + (lane & 15)];
-            }
-          } else {
-            float* out = reinterpret_cast<float*>(p.out[kind]);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) st[lane * 33 + j] = v[j];
-            __syncwarp();
-            // one row of 128 bytes per store
-            const size_t col = (size_t)n * BN + (size_t)c + (size_t)lane;
-#pragma unroll 4
-            for (int r = 0; r < 32; ++r)
-              if (r < rows_left) out[(row_base + r) * ld + col] = bits_f(st[r * 33 + lane]);
-          }
+          for (int r = 0; r < 32; ++r)
+            if (r < rows_left) out[(row_base + r) * ld + col] = bits_f(st[r * 33 + lane]);
           __syncwarp();
         }
       }
@@ -781,10 +720,6 @@ cudaError_t launch_gemm_tc(const moe_config_t& c, const ExpertArgs& a, int which
   p2.u_map[1] = p2.b_map[1];
   p2.out[0] = a.y_perm;
   p2.out[1] = a.y_shared;
-  p2.oexp[0] = a.y_exp;
-  p2.oexp[1] = a.y_exp ? a.ys_exp : nullptr;
-  p2.exp_rows[0] = A;
-  p2.exp_rows[1] = T;
   p2.ld_out[0] = d;
   p2.ld_out[1] = d;
   p2.K[0] = F;

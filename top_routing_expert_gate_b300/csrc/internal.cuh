@@ -54,8 +54,6 @@ struct WsLayout {
   size_t ec_scores;   // [E, T] fp32 (expert choice)
   size_t ec_w;        // [E, C] fp32 (expert choice)
   size_t ec_rowmap;   // [T, E] int32 (expert choice)
-  size_t y_exp;       // [d/32, A] uint8: exponents of the fp16 down-projection rows
-  size_t ys_exp;      // [d/32, T] uint8: the same for the shared expert
   size_t total;
   int nb;             // dispatch blocks
 };
@@ -183,13 +181,6 @@ cudaError_t launch_invert_perm(const moe_config_t& c, const int32_t* perm,
                                const int32_t* offsets, int32_t* row_of, int32_t* status,
                                cudaStream_t s, LaunchCounter* lc = nullptr);
 
-// The same from fp16 rows with per-32-column exponent bytes (ExpertArgs::y_exp).
-cudaError_t launch_combine_h(const moe_config_t& c, const void* y_perm, const uint8_t* y_exp,
-                             int rows, const float* topk_w, const int32_t* row_of,
-                             const uint8_t* drop_mask, const void* y_shared,
-                             const uint8_t* ys_exp, const float* shared_w, void* y,
-                             int32_t* status, cudaStream_t s, LaunchCounter* lc = nullptr);
-
 // y[t] = sum_j kept g[t,j] y_perm[row_of[t*k+j]] (+ w_s[t] * y_shared[t], w_s = 1 when
 // shared_w is null).
 cudaError_t launch_combine(const moe_config_t& c, const float* y_perm, const float* topk_w,
@@ -210,11 +201,6 @@ struct ExpertArgs {
   void* h_shared;       // [T, F_s]
   float* y_perm;        // [A, d]
   float* y_shared;      // [T, d]
-  // set: the tokens-in-M down GEMM stores y_perm / y_shared as fp16 rows
-  // ([A, d] / [T, d] halves) and one exponent byte per 32-column chunk,
-  // y_exp[c * A + r] / ys_exp[c * T + t] = 127 + s, the values being fp16 * 2^s
-  uint8_t* y_exp = nullptr;
-  uint8_t* ys_exp = nullptr;
   int32_t* status;
   const moe_weight_scales_t* scales = nullptr;   // E4M3 weights only
   int rows = 0;                                  // grouped rows (0: T * top_k)

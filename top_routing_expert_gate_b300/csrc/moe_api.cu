@@ -48,8 +48,6 @@ WsLayout ws_layout(const moe_config_t& c) {
   L.ec_scores = take(ec ? E * T * 4 : 0);
   L.ec_w = take(ec ? R * 4 : 0);
   L.ec_rowmap = take(ec ? T * E * 4 : 0);
-  L.y_exp = take(ec ? 0 : (d / 32) * A);
-  L.ys_exp = take(ec ? 0 : (d / 32) * T);
   L.total = o;
   return L;
 }
@@ -527,24 +525,11 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
   a.ev_up = ev ? ev[MOE_STAGE_GATE_UP] : nullptr;
   a.ev_down = ev ? ev[MOE_STAGE_DOWN] : nullptr;
   a.launches = &lc;
-  // Inside the fused call the down-projection rows only feed the combine, so
-  // the tokens-in-M down GEMM stores them as fp16 with one power-of-two
-  // exponent per 32 columns (half the bytes of fp32, relative error 2^-11
-  // per value); the split entry points keep fp32 rows.
-  const bool half_y = !ec && c.act_dtype == MOE_BF16 && c.weight_format == MOE_WEIGHTS_ACT &&
-                      !weights_in_m(c, kGemmDown);
-  if (half_y) {
-    a.y_exp = at<uint8_t>(ws, L.y_exp);
-    a.ys_exp = has_shared ? at<uint8_t>(ws, L.ys_exp) : nullptr;
-  }
   MOE_TRY_CUDA(run_experts(c, a, at<char>(ws, L.x_perm), s));
   MOE_TRY_CUDA(mark(MOE_STAGE_COMBINE));
   if (ec)
     MOE_TRY_CUDA(launch_ec_combine(c, a.y_perm, at<int32_t>(ws, L.ec_rowmap), ec_w, a.y_shared,
                                    shared_w, y, status, s, &lc));
-  else if (half_y)
-    MOE_TRY_CUDA(launch_combine_h(c, a.y_perm, a.y_exp, a.rows, g, row_of, dmask, a.y_shared,
-                                  a.ys_exp, shared_w, y, status, s, &lc));
   else
     MOE_TRY_CUDA(
         launch_combine(c, a.y_perm, g, row_of, dmask, a.y_shared, shared_w, y, status, s, &lc));
