@@ -71,7 +71,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 
 
 HEADLINE = "dsv3_prefill"
-PER_CONFIG = ("mixtral", "dsv3_decode", "switch")
+PER_CONFIG = ("mixtral", "dsv3_decode", "switch", "dsv3_decode_fp8")
 
 
 def parse_args(argv=None):

@@ -50,10 +50,20 @@ FP8_SHAPES = {
     "tm_capacity": _shape(T=700, d=256, E=8, k=2, F=256, capacity_factor=1.0, zipf_s=1.2),
 }
 
-# MOE_B300_FP8_LAYOUT: tokens in M (weights widened in shared memory) or
-# weights in M (widened into tensor memory) with token tiles of 64 or 128
-# rows; shapes the second kernel does not support fall back to the first
-FP8_LAYOUTS = ["tokens_m", "weights_tm", "weights_tm128"]
+# MOE_B300_FP8_LAYOUT: tokens in M (weights widened to bf16 in shared
+# memory) or weights in M (widened into tensor memory) with token tiles of 64
+# or 128 rows, whose operands are fp16 (tokens rescaled per row) or, with
+# MOE_B300_FP8_TOKENS=bf16, bf16; shapes the weights-in-M kernel does not
+# support fall back to tokens in M
+FP8_LAYOUTS = ["tokens_m", "weights_tm", "weights_tm128", "weights_tm_bf16"]
+
+
+def _set_fp8_layout(monkeypatch, layout):
+    monkeypatch.setenv("MOE_B300_FP8_LAYOUT", layout.replace("_bf16", ""))
+    if layout.endswith("_bf16"):
+        monkeypatch.setenv("MOE_B300_FP8_TOKENS", "bf16")
+    else:
+        monkeypatch.delenv("MOE_B300_FP8_TOKENS", raising=False)
 
 
 def _check_layer(s, inp, cfg, ws, out):
@@ -81,7 +91,7 @@ def _check_layer(s, inp, cfg, ws, out):
 @pytest.mark.parametrize("layout", FP8_LAYOUTS)
 @pytest.mark.parametrize("name", list(FP8_SHAPES))
 def test_fp8_layer_matches_oracle_all_tokens(name, layout, monkeypatch):
-    monkeypatch.setenv("MOE_B300_FP8_LAYOUT", layout)
+    _set_fp8_layout(monkeypatch, layout)
     s = FP8_SHAPES[name]
     inp = make_inputs(s, device=DEV, seed=11)
     assert inp["w_gate"].dtype == torch.float8_e4m3fn
@@ -105,7 +115,7 @@ def _every_code(shape_, gen):
 def test_fp8_every_code_decodes_like_the_oracle(layout, monkeypatch):
     # weights made of all 254 finite codes (subnormals, 448, both signs) with
     # non-power-of-two scales; the layer must match the oracle's decoding
-    monkeypatch.setenv("MOE_B300_FP8_LAYOUT", layout)
+    _set_fp8_layout(monkeypatch, layout)
     s = _shape(T=200, d=256, E=2, k=2, F=256, gate="sigmoid", rsf=2.5)
     inp = make_inputs(s, device=DEV, seed=12)
     g = torch.Generator().manual_seed(3)
@@ -125,7 +135,7 @@ def test_fp8_every_code_decodes_like_the_oracle(layout, monkeypatch):
 def test_fp8_equals_bf16_on_decoded_weights_with_power_of_two_scales(F_s, layout, monkeypatch):
     # the bf16 layer runs with the same MMA orientation (weights in M for the
     # tensor-memory kernel), so the products and sums are the same
-    monkeypatch.setenv("MOE_B300_FP8_LAYOUT", layout)
+    _set_fp8_layout(monkeypatch, layout)
     monkeypatch.setenv("MOE_B300_EXPERT_LAYOUT", "tokens_m" if layout == "tokens_m" else "weights_m")
     s = _shape(T=515, d=256, E=8, k=2, F=256, F_s=F_s, gate="sigmoid", rsf=2.5)
     inp = make_inputs(s, device=DEV, seed=13)

@@ -38,7 +38,20 @@
 // Tensor memory: columns [0, 256) two widened-A stages of 128 columns
 // (half h at +64h); [256, 512) the accumulators, 2 x TN columns per buffer
 // (half h at +TN·h, one column per token).
+//
+// fp16 operands (the default): the hardware widens two E4M3 codes to fp16x2
+// in one conversion, where bf16 needs a byte permute, shifts, masks and a
+// rebiasing multiply per pair, and the widening is what bounds this kernel.
+// The MMA then takes fp16 tokens too (A and B of one kind::f16 MMA share a
+// type): rows_to_f16 writes each token row (and later each row of h) as
+// fp16 * 2^s, with s per row chosen so that the row's largest magnitude lands
+// in [2^14, 2^15) - exact for every bf16 value of the row down to 2^-31 of
+// its largest - and the epilogue multiplies each token's accumulator by 2^s
+// before the weight scale.  Products and sums are then the bf16 path's,
+// scaled by powers of two.
 #include "fp8_common.cuh"
+
+#include <cuda_fp16.h>
 
 namespace moe {
 namespace {
@@ -98,6 +111,12 @@ struct MParams {
   int has_shared;
   int32_t* status;
   uint64_t timeout_ns;
+  // fp16 token rows: the accumulator of token column c of a tile is
+  // multiplied by row_scale[kind][r], r being the tile's row (routed rows of
+  // gate/up: the token perm[row] / perm_div)
+  const float* row_scale[2];
+  const int32_t* perm;
+  int perm_div;
 };
 
 __device__ __forceinline__ int m_n_tiles(int mode, int N) {
@@ -135,7 +154,7 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-template <int MODE, int TN>
+template <int MODE, int TN, bool F16>
 __global__ void __launch_bounds__(kMThreads, 1)
 grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
   using C = TmTile<TN>;
@@ -250,6 +269,15 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
   };
   // tokens of the tile, rounded up to 16 (the MMA's N and the rows loaded)
   auto tile_n = [&](int g, int m) { return (min(MTN, s_rows[g] - m * MTN) + 15) & ~15; };
+  // power of two of an fp16 token row (row = grouped row, or token for the shared group)
+  auto token_scale = [&](int kind, size_t row) -> float {
+    if (MODE == kMGateUp && kind == 0) {
+      const int a = __ldg(p.perm + row);
+      const int tok = a / p.perm_div;
+      row = a < 0 || tok >= p.T ? 0 : (size_t)tok;   // the gather reports a bad row
+    }
+    return __ldg(p.row_scale[kind] + row);
+  };
 
   bool failed = false;
   if (warp == 0) {
@@ -301,7 +329,8 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
         decode(t, g, m, n);
         const int kind = g < p.E ? 0 : 1;
         const int nk = p.K[kind] / MBK;
-        const uint32_t idesc = idesc_bf16_f32(MBM, (uint32_t)tile_n(g, m));
+        const uint32_t idesc = F16 ? idesc_f16_f32(MBM, (uint32_t)tile_n(g, m))
+                                   : idesc_bf16_f32(MBM, (uint32_t)tile_n(g, m));
         const int buf = local % NACC;
         const uint32_t acc_phase = (uint32_t)(local / NACC) & 1u;
         if (!mbar_wait(acce_bar(buf), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
@@ -424,10 +453,17 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const uint4 w = v[4 * h2 + c];
-            e4m3x4_to_bf16x4(w.x, o[8 * c + 0], o[8 * c + 1]);
-            e4m3x4_to_bf16x4(w.y, o[8 * c + 2], o[8 * c + 3]);
-            e4m3x4_to_bf16x4(w.z, o[8 * c + 4], o[8 * c + 5]);
-            e4m3x4_to_bf16x4(w.w, o[8 * c + 6], o[8 * c + 7]);
+            if (F16) {
+              e4m3x4_to_f16x4(w.x, o[8 * c + 0], o[8 * c + 1]);
+              e4m3x4_to_f16x4(w.y, o[8 * c + 2], o[8 * c + 3]);
+              e4m3x4_to_f16x4(w.z, o[8 * c + 4], o[8 * c + 5]);
+              e4m3x4_to_f16x4(w.w, o[8 * c + 6], o[8 * c + 7]);
+            } else {
+              e4m3x4_to_bf16x4(w.x, o[8 * c + 0], o[8 * c + 1]);
+              e4m3x4_to_bf16x4(w.y, o[8 * c + 2], o[8 * c + 3]);
+              e4m3x4_to_bf16x4(w.z, o[8 * c + 4], o[8 * c + 5]);
+              e4m3x4_to_bf16x4(w.w, o[8 * c + 6], o[8 * c + 7]);
+            }
           }
           tmem_st_32x32b_x32(t_row + (uint32_t)(ts * 128 + 32 * h2), o);
         }
@@ -477,14 +513,25 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
         const int lo = part * (MTN / 2), hi = min(n_valid, lo + MTN / 2);
 #pragma unroll 1
         for (int c0 = lo; c0 < hi; c0 += 16) {
+          // the 16 tokens' row scales: lane i fetches token c0 + (i & 15)'s,
+          // then each is broadcast from its lane
+          float rs_lane = 1.f;
+          if (F16 && c0 + (lane & 15) < hi)
+            rs_lane = token_scale(kind, row_base + (size_t)(c0 + (lane & 15)));
           uint32_t gv[16], uv[16];
           tmem_ld_32x32b_x16(tacc + (uint32_t)c0, gv);
           tmem_ld_32x32b_x16(tacc + (uint32_t)(MTN + c0), uv);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
+            const float rs = F16 ? __shfl_sync(0xffffffffu, rs_lane, j) : 1.f;
             if (c0 + j < hi) {
-              const float hv = silu_f(bits_f(gv[j]) * sg) * (bits_f(uv[j]) * su);
+              float gj = bits_f(gv[j]), uj = bits_f(uv[j]);
+              if (F16) {
+                gj *= rs;
+                uj *= rs;
+              }
+              const float hv = silu_f(gj * sg) * (uj * su);
               out[(row_base + (size_t)(c0 + j)) * ld + col] = __float2bfloat16_rn(hv);
             }
           }
@@ -497,12 +544,21 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
           const float sd = __ldg(p.b_scale[kind] + srow + col);
 #pragma unroll 1
           for (int c0 = 0; c0 < n_valid; c0 += 16) {
+            float rs_lane = 1.f;
+            if (F16 && c0 + (lane & 15) < n_valid)
+              rs_lane = token_scale(kind, row_base + (size_t)(c0 + (lane & 15)));
             uint32_t v[16];
             tmem_ld_32x32b_x16(tacc + (uint32_t)(hf * MTN + c0), v);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < n_valid) out[(row_base + (size_t)(c0 + j)) * ld + col] = bits_f(v[j]) * sd;
+            for (int j = 0; j < 16; ++j) {
+              const float rs = F16 ? __shfl_sync(0xffffffffu, rs_lane, j) : 1.f;
+              if (c0 + j < n_valid) {
+                float vj = bits_f(v[j]);
+                if (F16) vj *= rs;
+                out[(row_base + (size_t)(c0 + j)) * ld + col] = vj * sd;
+              }
+            }
           }
         }
       }
@@ -524,26 +580,64 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
   }
 }
 
-template <int MODE, int TN>
+template <int MODE, int TN, bool F16>
 cudaError_t launch_m(const MParams& p, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(grouped_gemm_fp8_tm_kernel<MODE, TN>,
+    attr_err = cudaFuncSetAttribute(grouped_gemm_fp8_tm_kernel<MODE, TN, F16>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     TmTile<TN>::kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  grouped_gemm_fp8_tm_kernel<MODE, TN><<<num_sms(), kMThreads, TmTile<TN>::kSmem, s>>>(p);
+  grouped_gemm_fp8_tm_kernel<MODE, TN, F16><<<num_sms(), kMThreads, TmTile<TN>::kSmem, s>>>(p);
   return cudaGetLastError();
+}
+
+// Row r of `in` (bf16, vec 8-element vectors per row) -> `out` (fp16, may be
+// `in` itself) as in[r] * 2^-s with s = clamp(floor(log2 max|in[r]|) - 14,
+// -126, 113), so the row's largest magnitude lands in [2^14, 2^15);
+// scale[r] = 2^s.  One warp per row: the maximum first, then the rewrite.
+__global__ void __launch_bounds__(256)
+rows_to_f16_kernel(const uint4* in, uint4* out, float* __restrict__ scale, int rows, int vec) {
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x >> 5;
+  for (int r = blockIdx.x * warps + (threadIdx.x >> 5); r < rows; r += gridDim.x * warps) {
+    const uint4* src = in + (size_t)r * vec;
+    uint32_t mx = 0;   // bf16 magnitudes compare as integers
+    for (int v = lane; v < vec; v += 32) {
+      const uint4 u = src[v];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mx = max(mx, max(w[i] & 0x7fffu, (w[i] >> 16) & 0x7fffu));
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    const int s = mx == 0 ? 0 : min(max((int)(mx >> 7) - 127 - 14, -126), 113);
+    const float down = __int_as_float((127 - s) << 23);   // 2^-s
+    uint4* dst = out + (size_t)r * vec;
+    for (int v = lane; v < vec; v += 32) {
+      const uint4 u = src[v];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float lo = __uint_as_float(w[i] << 16) * down;
+        const float hi = __uint_as_float(w[i] & 0xffff0000u) * down;
+        __half2 h = __floats2half2_rn(lo, hi);
+        o[i] = *reinterpret_cast<uint32_t*>(&h);
+      }
+      dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (lane == 0) scale[r] = __int_as_float((127 + s) << 23);
+  }
 }
 
 // Token boxes of tn, tn/2, .., 16 rows (64-element rows, 128-byte swizzle).
 bool token_maps_m(CUtensorMap (&m)[kMMaxBoxes], const void* ptr, uint64_t inner, uint64_t rows,
-                  int tn) {
+                  int tn, bool f16) {
   bool ok = true;
   for (int b = 0; b < kMMaxBoxes; ++b)
-    if ((tn >> b) >= 16) ok &= make_map(&m[b], ptr, inner, rows, (uint32_t)(tn >> b));
+    if ((tn >> b) >= 16) ok &= make_map(&m[b], ptr, inner, rows, (uint32_t)(tn >> b), f16);
   return ok;
 }
 
@@ -568,10 +662,22 @@ bool fp8_tm_supported(const moe_config_t& c) {
   return c.d_model % 256 == 0 && c.d_ff % 128 == 0 && shared_ok;
 }
 
+cudaError_t launch_rows_to_f16(const void* in, void* out, float* scale, int rows, int cols,
+                               cudaStream_t s, LaunchCounter* lc) {
+  if (rows == 0) return cudaSuccess;
+  int blocks = (rows + 7) / 8;
+  if (blocks > num_sms() * 8) blocks = num_sms() * 8;
+  rows_to_f16_kernel<<<blocks, 256, 0, s>>>((const uint4*)in, (uint4*)out, scale, rows,
+                                            cols / 8);
+  count_launch(lc);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gemm_fp8_tm(const moe_config_t& c, const ExpertArgs& a, int which, int tn,
                                cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
   if (!fp8_tm_supported(c) || (tn != 64 && tn != 128)) return cudaErrorInvalidValue;
+  const bool f16 = a.tok_scale != nullptr;
   const int T = c.T, E = c.n_experts, d = c.d_model, F = c.d_ff, Fs = c.d_ff_shared;
   const int A = a.rows > 0 ? a.rows : T * c.top_k;
   const bool has_shared = Fs > 0 && a.ws_gate != nullptr;
@@ -585,9 +691,13 @@ cudaError_t launch_gemm_fp8_tm(const moe_config_t& c, const ExpertArgs& a, int w
   p.has_shared = has_shared ? 1 : 0;
   p.status = a.status;
   p.timeout_ns = kWaitTimeoutNs;
+  p.perm = a.perm;
+  p.perm_div = a.perm_div > 0 ? a.perm_div : 1;
   if (which == kGemmGateUp) {
-    ok &= token_maps_m(p.a_map[0], a.x_perm, d, A, tn);
-    ok &= token_maps_m(p.a_map[1], a.x, d, T, tn);
+    ok &= token_maps_m(p.a_map[0], a.x_perm, d, A, tn, f16);
+    ok &= token_maps_m(p.a_map[1], a.x, d, T, tn, f16);
+    p.row_scale[0] = a.tok_scale;
+    p.row_scale[1] = a.tok_scale;
     ok &= make_map_e4m3_sw128(&p.b_map[0], a.w_gate, d, (uint64_t)E * F);
     ok &= make_map_e4m3_sw128(&p.u_map[0], a.w_up, d, (uint64_t)E * F);
     p.b_scale[0] = sc.gate_scale;
@@ -613,11 +723,13 @@ cudaError_t launch_gemm_fp8_tm(const moe_config_t& c, const ExpertArgs& a, int w
     p.N[1] = has_shared ? Fs : 128;
     p.b_rows_per_expert = F;
   } else {
-    ok &= token_maps_m(p.a_map[0], a.h, F, A, tn);
+    ok &= token_maps_m(p.a_map[0], a.h, F, A, tn, f16);
     ok &= make_map_e4m3_sw128(&p.b_map[0], a.w_down, F, (uint64_t)E * d);
     p.b_scale[0] = sc.down_scale;
+    p.row_scale[0] = a.h_scale;
+    p.row_scale[1] = a.hs_scale;
     if (has_shared) {
-      ok &= token_maps_m(p.a_map[1], a.h_shared, Fs, T, tn);
+      ok &= token_maps_m(p.a_map[1], a.h_shared, Fs, T, tn, f16);
       ok &= make_map_e4m3_sw128(&p.b_map[1], a.ws_down, Fs, d);
       p.b_scale[1] = sc.shared_down_scale;
     } else {
@@ -641,10 +753,18 @@ cudaError_t launch_gemm_fp8_tm(const moe_config_t& c, const ExpertArgs& a, int w
   }
   if (!ok) return cudaErrorInvalidValue;
   cudaError_t err;
-  if (tn == 64)
-    err = which == kGemmGateUp ? launch_m<kMGateUp, 64>(p, s) : launch_m<kMDown, 64>(p, s);
-  else
-    err = which == kGemmGateUp ? launch_m<kMGateUp, 128>(p, s) : launch_m<kMDown, 128>(p, s);
+  const bool up = which == kGemmGateUp;
+  if (f16) {
+    if (tn == 64)
+      err = up ? launch_m<kMGateUp, 64, true>(p, s) : launch_m<kMDown, 64, true>(p, s);
+    else
+      err = up ? launch_m<kMGateUp, 128, true>(p, s) : launch_m<kMDown, 128, true>(p, s);
+  } else {
+    if (tn == 64)
+      err = up ? launch_m<kMGateUp, 64, false>(p, s) : launch_m<kMDown, 64, false>(p, s);
+    else
+      err = up ? launch_m<kMGateUp, 128, false>(p, s) : launch_m<kMDown, 128, false>(p, s);
+  }
   count_launch(a.launches);
   return err;
 }

@@ -33,6 +33,14 @@ __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint3
   hi = e4m3x2_hi_to_bf16x2(prmt_zero(w, 0x3424u));
 }
 
+// Four codes (one 32-bit word, code j in byte j) -> fp16x2 of codes 0,1 and
+// 2,3 with the hardware conversion (every finite E4M3 value is exact in
+// fp16, subnormal codes included).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"((unsigned short)(w & 0xffffu)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"((unsigned short)(w >> 16)));
+}
+
 // Bounded mbarrier wait in every lane; the warp agrees on the outcome.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
                                           uint64_t timeout_ns) {

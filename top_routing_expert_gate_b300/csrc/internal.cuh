@@ -54,6 +54,10 @@ struct WsLayout {
   size_t ec_scores;   // [E, T] fp32 (expert choice)
   size_t ec_w;        // [E, C] fp32 (expert choice)
   size_t ec_rowmap;   // [T, E] int32 (expert choice)
+  size_t x16;         // [T, d] fp16 (E4M3 weights with fp16 operands)
+  size_t tok_scale;   // [T] fp32
+  size_t h_scale;     // [A] fp32
+  size_t hs_scale;    // [T] fp32
   size_t total;
   int nb;             // dispatch blocks
 };
@@ -195,6 +199,12 @@ struct ExpertArgs {
   const void* x_perm;   // [A, d], built by the gather in run_experts
   const int32_t* offsets;
   const int32_t* perm = nullptr;   // grouped row -> assignment (token choice) or token
+  int perm_div = 0;                // perm[r] / perm_div is the token of grouped row r
+  // E4M3 weights with fp16 operands: x, x_perm, h and h_shared hold fp16
+  // rows, each row's values times its power-of-two scale below
+  const float* tok_scale = nullptr;   // [T] per token (x, and x_perm through perm)
+  const float* h_scale = nullptr;     // [A] per grouped row of h
+  const float* hs_scale = nullptr;    // [T] per row of h_shared
   const void* w_gate; const void* w_up; const void* w_down;
   const void* ws_gate; const void* ws_up; const void* ws_down;
   void* h;              // [A, F]
@@ -226,6 +236,10 @@ cudaError_t launch_gemm_fp8w(const moe_config_t& c, const ExpertArgs& a, int whi
 // 128 rows; needs fp8_tm_supported(c): d_model % 256, d_ff % 128 and
 // d_ff_shared % 128 == 0.
 bool fp8_tm_supported(const moe_config_t& c);
+// rows x cols bf16 -> fp16 * 2^s per row (out may alias in), scale[r] = 2^s
+// (rows_to_f16_kernel, experts_fp8_tm.cu); cols a multiple of 8.
+cudaError_t launch_rows_to_f16(const void* in, void* out, float* scale, int rows, int cols,
+                               cudaStream_t s, LaunchCounter* lc = nullptr);
 cudaError_t launch_gemm_fp8_tm(const moe_config_t& c, const ExpertArgs& a, int which, int tn,
                                cudaStream_t s);
 

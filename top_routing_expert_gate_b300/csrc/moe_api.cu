@@ -48,6 +48,11 @@ WsLayout ws_layout(const moe_config_t& c) {
   L.ec_scores = take(ec ? E * T * 4 : 0);
   L.ec_w = take(ec ? R * 4 : 0);
   L.ec_rowmap = take(ec ? T * E * 4 : 0);
+  const bool f8 = c.weight_format == MOE_WEIGHTS_FP8_E4M3;
+  L.x16 = take(f8 ? T * d * 2 : 0);
+  L.tok_scale = take(f8 ? T * 4 : 0);
+  L.h_scale = take(f8 ? R * 4 : 0);
+  L.hs_scale = take(f8 ? T * 4 : 0);
   L.total = o;
   return L;
 }
@@ -64,6 +69,25 @@ inline P* at(void* ws, size_t off) {
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Scratch the E4M3 weights-in-M kernel uses for fp16 operands (workspace).
+struct F16Rows {
+  void* x16 = nullptr;         // [T, d]
+  float* tok_scale = nullptr;  // [T]
+  float* h_scale = nullptr;    // [A]
+  float* hs_scale = nullptr;   // [T]
+};
+
+F16Rows f16_rows(const moe_config_t& c, void* ws, const WsLayout& L) {
+  F16Rows f;
+  if (c.weight_format == MOE_WEIGHTS_FP8_E4M3) {
+    f.x16 = at<char>(ws, L.x16);
+    f.tok_scale = at<float>(ws, L.tok_scale);
+    f.h_scale = at<float>(ws, L.h_scale);
+    f.hs_scale = at<float>(ws, L.hs_scale);
+  }
+  return f;
+}
 
 // Shape/option checks shared by every call.
 moe_status_t check_config(const moe_config_t* c) {
@@ -167,11 +191,26 @@ int fp8_tmem_tile(const moe_config_t& c) {
   return (int64_t)c.T * c.top_k <= (int64_t)64 * c.n_experts && c.T <= 256 ? 64 : 128;
 }
 
-// The gather (x_perm[r] = x[perm[r] / div]) and the two grouped GEMMs.
-cudaError_t run_experts(const moe_config_t& c, ExpertArgs a, void* x_perm, cudaStream_t s) {
+// The gather (x_perm[r] = x[perm[r] / div]) and the two grouped GEMMs.  With
+// E4M3 weights in the weights-in-M kernel the tokens become fp16 rows first
+// (x, then h after gate/up), unless MOE_B300_FP8_TOKENS=bf16 (a test and
+// tuning override) keeps the bf16 operands.
+cudaError_t run_experts(const moe_config_t& c, ExpertArgs a, void* x_perm, cudaStream_t s,
+                        const F16Rows& f16) {
   const bool fp8 = c.weight_format == MOE_WEIGHTS_FP8_E4M3;
   const int fp8_tn = fp8 ? fp8_tmem_tile(c) : 0;
   const int div = c.routing == MOE_ROUTE_EXPERT_CHOICE ? 1 : c.top_k;
+  const char* tok_env = getenv("MOE_B300_FP8_TOKENS");
+  const bool half_ops =
+      fp8_tn > 0 && f16.x16 != nullptr && !(tok_env && strcmp(tok_env, "bf16") == 0);
+  a.perm_div = div;
+  if (half_ops) {
+    const cudaError_t e =
+        launch_rows_to_f16(a.x, f16.x16, f16.tok_scale, c.T, c.d_model, s, a.launches);
+    if (e != cudaSuccess) return e;
+    a.x = f16.x16;
+    a.tok_scale = f16.tok_scale;
+  }
   {
     const cudaError_t e = launch_gather(c, a.x, a.perm, a.offsets, x_perm, a.status, s,
                                         a.launches, div);
@@ -180,6 +219,16 @@ cudaError_t run_experts(const moe_config_t& c, ExpertArgs a, void* x_perm, cudaS
   }
   if (c.act_dtype != MOE_BF16) return launch_experts_simt(c, a, s);
   for (int which = kGemmGateUp; which <= kGemmDown; ++which) {
+    if (half_ops && which == kGemmDown) {
+      // h and h_shared rewritten in place as fp16 rows
+      cudaError_t e = launch_rows_to_f16(a.h, a.h, f16.h_scale, a.rows, c.d_ff, s, a.launches);
+      if (e == cudaSuccess && a.ws_gate)
+        e = launch_rows_to_f16(a.h_shared, a.h_shared, f16.hs_scale, c.T, c.d_ff_shared, s,
+                               a.launches);
+      if (e != cudaSuccess) return e;
+      a.h_scale = f16.h_scale;
+      a.hs_scale = f16.hs_scale;
+    }
     cudaEvent_t ev = which == kGemmGateUp ? a.ev_up : a.ev_down;
     if (ev) {
       const cudaError_t e = cudaEventRecord(ev, s);
@@ -383,7 +432,7 @@ moe_status_t moe_grouped_swiglu(const moe_config_t* cfg, const void* x, const in
   a.status = status;
   a.scales = scales;
   a.rows = (int)grouped_rows(*cfg);
-  return cuda_status(run_experts(*cfg, a, at<char>(ws, L.x_perm), s));
+  return cuda_status(run_experts(*cfg, a, at<char>(ws, L.x_perm), s, f16_rows(*cfg, ws, L)));
 }
 
 moe_status_t moe_combine(const moe_config_t* cfg, const float* y_perm, const float* topk_w,
@@ -525,7 +574,7 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x, const vo
   a.ev_up = ev ? ev[MOE_STAGE_GATE_UP] : nullptr;
   a.ev_down = ev ? ev[MOE_STAGE_DOWN] : nullptr;
   a.launches = &lc;
-  MOE_TRY_CUDA(run_experts(c, a, at<char>(ws, L.x_perm), s));
+  MOE_TRY_CUDA(run_experts(c, a, at<char>(ws, L.x_perm), s, f16_rows(c, ws, L)));
   MOE_TRY_CUDA(mark(MOE_STAGE_COMBINE));
   if (ec)
     MOE_TRY_CUDA(launch_ec_combine(c, a.y_perm, at<int32_t>(ws, L.ec_rowmap), ec_w, a.y_shared,

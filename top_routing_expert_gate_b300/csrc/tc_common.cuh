@@ -291,6 +291,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// The same with A and B fp16 (format 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
 __device__ __forceinline__ float bits_f(uint32_t u) { return __uint_as_float(u); }
 
 // SiLU(g) = g * sigmoid(g) = g / (1 + e^-g) in fp32 with the fast reciprocal
@@ -317,17 +322,19 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // Row-major bf16 matrix [rows, inner] read in boxes of 64 (one 128-byte
 // swizzle span) x box_rows with the 128-byte swizzle; rows past the end read
 // as zero.
+// (fp16 = true: the same for an fp16 matrix.)
 inline bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows,
-                     uint32_t box_rows) {
+                     uint32_t box_rows, bool fp16 = false) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {inner * 2};
   cuuint32_t box[2] = {64u, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 inline int num_sms() {
