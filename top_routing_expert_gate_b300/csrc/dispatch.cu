@@ -81,24 +81,15 @@ __global__ void dispatch_scan_kernel(const int32_t* __restrict__ block_hist, int
   }
 }
 
-// Stable scatter: slot(a) = #{a' < a : idx[a'] == idx[a]}.
-__global__ void __launch_bounds__(kDispatchThreads)
-dispatch_scatter_kernel(const int32_t* __restrict__ idx, int A, int E, int capacity,
-                        const int32_t* __restrict__ block_base,
-                        const int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
-                        int32_t* __restrict__ row_of, uint8_t* __restrict__ drop_mask,
-                        int32_t* status) {
-  __shared__ int wc[32][kMaxExperts];   // per-warp counts, then prefixes
-  __shared__ int run[kMaxExperts];      // slots taken so far per expert
-  __shared__ int off[kMaxExperts];
+// Stable scatter of one chunk of assignments: slot(a) = #{a' < a : idx[a'] ==
+// idx[a]}, the chunk's running slot counts starting at run[] (shared, updated),
+// off[] the experts' first rows.
+__device__ __forceinline__ void scatter_chunk(const int32_t* __restrict__ idx, int A, int E,
+                                              int capacity, int a0, int (*wc)[kMaxExperts],
+                                              int* run, const int* off, int32_t* __restrict__ perm,
+                                              int32_t* __restrict__ row_of,
+                                              uint8_t* __restrict__ drop_mask) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int e = tid; e < E; e += blockDim.x) {
-    run[e] = block_base[(size_t)blockIdx.x * E + e];
-    off[e] = offsets[e];
-  }
-  for (int i = tid; i < 32 * kMaxExperts; i += blockDim.x) (&wc[0][0])[i] = 0;
-  __syncthreads();
-  const int a0 = blockIdx.x * kDispatchChunk;
   for (int r = 0; r < kRounds; ++r) {
     const int a = a0 + r * kDispatchThreads + tid;
     const int e = load_expert(idx, a, A, E, nullptr);
@@ -138,7 +129,73 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, int A, int E, int capac
     for (int i = tid; i < 32 * E; i += blockDim.x) wc[i / E][i % E] = 0;
     __syncthreads();
   }
-  (void)status;
+}
+
+// Stable scatter, one block per chunk, after the histogram and scan kernels.
+__global__ void __launch_bounds__(kDispatchThreads)
+dispatch_scatter_kernel(const int32_t* __restrict__ idx, int A, int E, int capacity,
+                        const int32_t* __restrict__ block_base,
+                        const int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                        int32_t* __restrict__ row_of, uint8_t* __restrict__ drop_mask) {
+  __shared__ int wc[32][kMaxExperts];   // per-warp counts, then prefixes
+  __shared__ int run[kMaxExperts];      // slots taken so far per expert
+  __shared__ int off[kMaxExperts];
+  const int tid = threadIdx.x;
+  for (int e = tid; e < E; e += blockDim.x) {
+    run[e] = block_base[(size_t)blockIdx.x * E + e];
+    off[e] = offsets[e];
+  }
+  for (int i = tid; i < 32 * kMaxExperts; i += blockDim.x) (&wc[0][0])[i] = 0;
+  __syncthreads();
+  scatter_chunk(idx, A, E, capacity, blockIdx.x * kDispatchChunk, wc, run, off, perm, row_of,
+                drop_mask);
+}
+
+// The whole dispatch of at most one chunk of assignments in one block:
+// histogram, capacity cut, offsets, scatter (the three kernels' steps).
+__global__ void __launch_bounds__(kDispatchThreads)
+dispatch_small_kernel(const int32_t* __restrict__ idx, int A, int E, int capacity,
+                      int32_t* __restrict__ counts, int32_t* __restrict__ drops,
+                      int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                      int32_t* __restrict__ row_of, uint8_t* __restrict__ drop_mask,
+                      int32_t* status) {
+  __shared__ int wc[32][kMaxExperts];
+  __shared__ int run[kMaxExperts];
+  __shared__ int off[kMaxExperts];   // histogram, then kept counts, then first rows
+  const int tid = threadIdx.x, lane = tid & 31;
+  for (int e = tid; e < E; e += blockDim.x) {
+    off[e] = 0;
+    run[e] = 0;
+  }
+  for (int i = tid; i < 32 * kMaxExperts; i += blockDim.x) (&wc[0][0])[i] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int e = load_expert(idx, r * kDispatchThreads + tid, A, E, status);
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&off[e], __popc(peers));
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    const int load = off[e];
+    const int kp = capacity >= 0 ? min(load, capacity) : load;
+    counts[e] = kp;
+    drops[e] = load - kp;
+    off[e] = kp;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int sum = 0;
+    for (int i = 0; i < E; ++i) {
+      const int kp = off[i];
+      off[i] = sum;
+      offsets[i] = sum;
+      sum += kp;
+    }
+    offsets[E] = sum;
+  }
+  __syncthreads();
+  scatter_chunk(idx, A, E, capacity, 0, wc, run, off, perm, row_of, drop_mask);
 }
 
 // One warp per grouped row, 16-byte vectors; row r holds token perm[r] / k.
@@ -204,18 +261,26 @@ __device__ __forceinline__ void store4(__nv_bfloat16* y, float4 v) {
   *(uint2*)y = u;
 }
 
-// One block per token (grid-stride); fp32 accumulation in ascending j, then
-// the shared expert (times its per-token gate when given); one write of y.
+// One block per (token, span of the row's four-column vectors), grid-stride:
+// a large batch takes whole rows (span = the row), a small one splits each row
+// into spans of 256 vectors so that it still spreads over the GPU.  fp32
+// accumulation in ascending j, then the shared expert (times its per-token
+// gate when given); one write of y.
+constexpr int kCombineVecs = 256;
 template <typename TOut>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kCombineVecs)
 combine_kernel(const float4* __restrict__ y_perm, const float* __restrict__ topk_w,
                const int32_t* __restrict__ row_of, const uint8_t* __restrict__ drop_mask,
                const float4* __restrict__ y_shared, const float* __restrict__ shared_w,
-               TOut* __restrict__ y, int T, int k, int d, int A, int32_t* status) {
+               TOut* __restrict__ y, int T, int k, int d, int A, int nch, int32_t* status) {
   __shared__ int s_row[kMaxTopK];
   __shared__ float s_g[kMaxTopK];
   const int d4 = d >> 2;
-  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+  const int span = (d4 + nch - 1) / nch;
+  for (int w = blockIdx.x; w < T * nch; w += gridDim.x) {
+    const int t = w / nch;
+    const int v0 = (w - t * nch) * span;
+    const int v1 = min(d4, v0 + span);
     if (threadIdx.x < k) {
       const int a = t * k + threadIdx.x;
       int r = -1;
@@ -230,7 +295,7 @@ combine_kernel(const float4* __restrict__ y_perm, const float* __restrict__ topk
       s_g[threadIdx.x] = topk_w[a];
     }
     __syncthreads();
-    for (int v = threadIdx.x; v < d4; v += blockDim.x) {
+    for (int v = v0 + (int)threadIdx.x; v < v1; v += blockDim.x) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int j = 0; j < k; ++j) {
         const int r = s_row[j];
@@ -283,6 +348,14 @@ cudaError_t launch_dispatch(const moe_config_t& c, const int32_t* idx, int32_t* 
                             LaunchCounter* lc) {
   const int A = c.T * c.top_k, E = c.n_experts;
   const int nb = (A + kDispatchChunk - 1) / kDispatchChunk;
+  if (nb == 1) {
+    // one chunk: the three steps in one block
+    dispatch_small_kernel<<<1, kDispatchThreads, 0, s>>>(idx, A, E, c.capacity, counts, drops,
+                                                         offsets, perm, row_of, drop_mask,
+                                                         status);
+    count_launch(lc);
+    return cudaGetLastError();
+  }
   if (nb > 0) {
     dispatch_hist_kernel<<<nb, kDispatchThreads, 0, s>>>(idx, A, E, block_hist, status);
     count_launch(lc);
@@ -295,8 +368,7 @@ cudaError_t launch_dispatch(const moe_config_t& c, const int32_t* idx, int32_t* 
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || nb == 0) return err;
   dispatch_scatter_kernel<<<nb, kDispatchThreads, 0, s>>>(idx, A, E, c.capacity, block_base,
-                                                          offsets, perm, row_of, drop_mask,
-                                                          status);
+                                                          offsets, perm, row_of, drop_mask);
   count_launch(lc);
   return cudaGetLastError();
 }
@@ -337,17 +409,19 @@ cudaError_t launch_combine(const moe_config_t& c, const float* y_perm, const flo
                            int32_t* status, cudaStream_t s, LaunchCounter* lc) {
   const int T = c.T;
   if (T == 0) return cudaSuccess;
-  int blocks = T;
+  // split rows only when the batch alone would not fill the GPU
+  const int nch = T < 2 * sm_count() ? (c.d_model / 4 + kCombineVecs - 1) / kCombineVecs : 1;
+  long long blocks = (long long)T * nch;
   if (blocks > sm_count() * 16) blocks = sm_count() * 16;
   const int A = T * c.top_k;
   if (c.out_dtype == MOE_BF16)
-    combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+    combine_kernel<__nv_bfloat16><<<(int)blocks, kCombineVecs, 0, s>>>(
         (const float4*)y_perm, topk_w, row_of, drop_mask, (const float4*)y_shared, shared_w,
-        (__nv_bfloat16*)y, T, c.top_k, c.d_model, A, status);
+        (__nv_bfloat16*)y, T, c.top_k, c.d_model, A, nch, status);
   else
-    combine_kernel<float><<<blocks, 256, 0, s>>>((const float4*)y_perm, topk_w, row_of,
-                                                 drop_mask, (const float4*)y_shared, shared_w, (float*)y,
-                                                 T, c.top_k, c.d_model, A, status);
+    combine_kernel<float><<<(int)blocks, kCombineVecs, 0, s>>>(
+        (const float4*)y_perm, topk_w, row_of, drop_mask, (const float4*)y_shared, shared_w,
+        (float*)y, T, c.top_k, c.d_model, A, nch, status);
   count_launch(lc);
   return cudaGetLastError();
 }
