@@ -91,6 +91,7 @@ __device__ __forceinline__ void scatter_chunk(const int32_t* __restrict__ idx, i
                                               uint8_t* __restrict__ drop_mask) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int r = 0; r < kRounds; ++r) {
+    if (a0 + r * kDispatchThreads >= A) break;   // the same for the whole block
     const int a = a0 + r * kDispatchThreads + tid;
     const int e = load_expert(idx, a, A, E, nullptr);
     const unsigned peers = __match_any_sync(0xffffffffu, e);
@@ -169,8 +170,7 @@ dispatch_small_kernel(const int32_t* __restrict__ idx, int A, int E, int capacit
   }
   for (int i = tid; i < 32 * kMaxExperts; i += blockDim.x) (&wc[0][0])[i] = 0;
   __syncthreads();
-#pragma unroll
-  for (int r = 0; r < kRounds; ++r) {
+  for (int r = 0; r < kRounds && r * kDispatchThreads < A; ++r) {
     const int e = load_expert(idx, r * kDispatchThreads + tid, A, E, status);
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&off[e], __popc(peers));
@@ -184,15 +184,35 @@ dispatch_small_kernel(const int32_t* __restrict__ idx, int A, int E, int capacit
     off[e] = kp;
   }
   __syncthreads();
-  if (tid == 0) {
+  if (tid < 32) {
+    // exclusive prefix of the kept counts: lane l sums experts
+    // [l*per, (l+1)*per), a warp scan gives each lane its start
+    constexpr int per = (kMaxExperts + 31) / 32;
+    int loc[per];
     int sum = 0;
-    for (int i = 0; i < E; ++i) {
-      const int kp = off[i];
-      off[i] = sum;
-      offsets[i] = sum;
-      sum += kp;
+#pragma unroll
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      loc[i] = e < E ? off[e] : 0;
+      sum += loc[i];
     }
-    offsets[E] = sum;
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run_e = incl - sum;
+#pragma unroll
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) {
+        off[e] = run_e;
+        offsets[e] = run_e;
+      }
+      run_e += loc[i];
+    }
+    if (lane == 31) offsets[E] = incl;
   }
   __syncthreads();
   scatter_chunk(idx, A, E, capacity, 0, wc, run, off, perm, row_of, drop_mask);
@@ -326,17 +346,6 @@ combine_kernel(const float4* __restrict__ y_perm, const float* __restrict__ topk
     }
     __syncthreads();
   }
-}
-
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      n = 148;
-  }
-  return n;
 }
 
 }  // namespace

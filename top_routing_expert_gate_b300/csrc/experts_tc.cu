@@ -567,21 +567,29 @@ router_gemm_kernel(const __grid_constant__ RouterParams p) {
     }
   } else {
     const int q = warp & 3;
-    const int row = q * 32 + lane;
-    const int t = m * BM + row;
+    const int t0 = m * BM + q * 32;   // first token of this warp's 32 TMEM lanes
     if (mbar_wait(accf, 0, abort_flag, p.timeout_ns)) {
       tc_fence_after();
-      float* out = p.partial + ((size_t)split * p.T + (size_t)t) * p.E;
+      // Every MMA has completed, so the token stages are free: each warp
+      // passes its 32 x 16 blocks through a padded tile there, so that a
+      // store writes 16 consecutive logits of one token row (two rows per
+      // warp instruction) instead of one logit in each of 32 rows.
+      float* st = reinterpret_cast<float*>(smem) + q * (32 * 17);
+      float* out = p.partial + ((size_t)split * p.T + (size_t)t0) * p.E;
+      const int rows = min(32, p.T - t0);
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16);
       for (int c = 0; c < p.E_pad; c += 16) {
         uint32_t v[16];
         tmem_ld_32x32b_x16(tbase + (uint32_t)c, v);
         tmem_ld_wait();
-        if (t < p.T) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c + j < p.E) out[c + j] = bits_f(v[j]);
-        }
+        for (int j = 0; j < 16; ++j) st[lane * 17 + j] = bits_f(v[j]);
+        __syncwarp();
+        const int col = c + (lane & 15);
+#pragma unroll 4
+        for (int r = lane >> 4; r < rows; r += 2)
+          if (col < p.E) out[(size_t)r * p.E + col] = st[r * 17 + (lane & 15)];
+        __syncwarp();
       }
     } else if (lane == 0) {
       *abort_flag = 1;

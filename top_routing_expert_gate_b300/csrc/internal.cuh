@@ -97,6 +97,18 @@ inline void count_launch(LaunchCounter* lc, int k = 1) {
 
 // fp32 router logits held as `splits` partial sums [splits][T][E] plus an
 // optional per-expert bias: z[t,e] = sum_s partials[s][t][e] (in s order) + bias[e].
+// Streaming multiprocessors of the current device (queried once).
+inline int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n = 148;
+  }
+  return n;
+}
+
 struct LogitsView {
   const float* partials;
   int splits;

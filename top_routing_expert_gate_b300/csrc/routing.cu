@@ -106,7 +106,7 @@ topk_gate_kernel(const float* __restrict__ partials, int splits, size_t split_st
                  int n_group, int topk_group, float* __restrict__ logits_out, int T, int E,
                  int k, int gate, int renorm, float rsf, int tpb, int32_t* __restrict__ idx_out,
                  float* __restrict__ w_out, float* __restrict__ mp_partial) {
-  __shared__ float red[8][kMaxExperts];
+  __shared__ float red[8][kMaxExperts];   // logits of the chunk's tokens, then score partials
   __shared__ float keys[SCORE_KEY ? 8 : 1][SCORE_KEY ? kMaxExperts : 1];   // per-warp ranking keys
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float acc[EPL];
@@ -115,20 +115,56 @@ topk_gate_kernel(const float* __restrict__ partials, int splits, size_t split_st
 
   const int t_begin = blockIdx.x * tpb;
   const int t_end = min(T, t_begin + tpb);
-  for (int t = t_begin + warp; t < t_end; t += 8) {
-    const float* row = partials + (size_t)t * E;
-    float zv[EPL], sc[EPL];
+  // With more than two split partials (a small batch), the whole block sums
+  // them first; otherwise each lane adds its own experts' partials.
+  const bool presum = splits > 2;
+  // chunks of 8 tokens, warp w taking token t0 + w
+  for (int t0 = t_begin; t0 < t_end; t0 += 8) {
+    const int nt = min(8, t_end - t0);
+    if (presum) {
+      // the chunk's logits: the whole block sums the split partials (in split
+      // order) for 8 tokens x E experts, every load independent of the others
+      __syncthreads();   // red[] of the previous chunk has been read
+      for (int j = threadIdx.x; j < nt * E; j += blockDim.x) {
+        const int tk = j / E, e = j - tk * E;
+        const float* src = partials + (size_t)(t0 + tk) * E + e;
+        float pv[kMaxRouterSplits];
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) {
-        float v = row[e];
-        for (int sp = 1; sp < splits; ++sp) v += row[(size_t)sp * split_stride + e];
+        for (int sp = 0; sp < kMaxRouterSplits; ++sp)
+          pv[sp] = sp < splits ? src[(size_t)sp * split_stride] : 0.f;
+        float v = pv[0];
+#pragma unroll
+        for (int sp = 1; sp < kMaxRouterSplits; ++sp)
+          if (sp < splits) v += pv[sp];
         if (bias) v += bias[e];
-        zv[i] = v;
-        if (logits_out) logits_out[(size_t)t * E + e] = v;
-      } else {
-        zv[i] = -INFINITY;
+        red[tk][e] = v;
+        if (logits_out) logits_out[(size_t)(t0 + tk) * E + e] = v;
+      }
+      __syncthreads();
+    }
+    const int t = t0 + warp;
+    if (warp >= nt) continue;
+    float zv[EPL], sc[EPL];
+    if (presum) {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        zv[i] = e < E ? red[warp][e] : -INFINITY;
+      }
+    } else {
+      const float* row = partials + (size_t)t * E;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) {
+          float v = row[e];
+          if (splits > 1) v += row[split_stride + e];
+          if (bias) v += bias[e];
+          zv[i] = v;
+          if (logits_out) logits_out[(size_t)t * E + e] = v;
+        } else {
+          zv[i] = -INFINITY;
+        }
       }
     }
     if (gate == MOE_GATE_SOFTMAX) {
@@ -255,6 +291,7 @@ topk_gate_kernel(const float* __restrict__ partials, int splits, size_t split_st
     }
   }
   if (mp_partial == nullptr) return;
+  __syncthreads();   // every warp is done with the last chunk's logits
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
@@ -413,10 +450,17 @@ cudaError_t launch_topk(const moe_config_t& c, const LogitsView& z, const float*
     if (mean_prob) return cudaMemsetAsync(mean_prob, 0, sizeof(float) * E, s);
     return cudaSuccess;
   }
-  int nblocks = (T + 7) / 8;
-  if (nblocks > kTopkMaxBlocks) nblocks = kTopkMaxBlocks;
-  const int tpb = (T + nblocks - 1) / nblocks;
-  nblocks = (T + tpb - 1) / tpb;
+  // up to 8 tokens per block (one per warp), fewer when the batch would
+  // not fill the GPU: the block sums a token's split partials with one
+  // thread per expert, so a small batch takes one block per token
+  int tpb = T / sm_count();
+  tpb = tpb < 1 ? 1 : (tpb > 8 ? 8 : tpb);
+  int nblocks = (T + tpb - 1) / tpb;
+  if (nblocks > kTopkMaxBlocks) {
+    nblocks = kTopkMaxBlocks;
+    tpb = (T + nblocks - 1) / nblocks;
+    nblocks = (T + tpb - 1) / tpb;
+  }
   float* part = mean_prob ? mp_partial : nullptr;
   const bool score_key = score_bias != nullptr || c.n_group > 1;
   const int ng = c.n_group > 1 ? c.n_group : 1;
