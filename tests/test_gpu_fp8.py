@@ -51,11 +51,12 @@ FP8_SHAPES = {
 }
 
 # MOE_B300_FP8_LAYOUT: tokens in M (weights widened to bf16 in shared
-# memory) or weights in M (widened into tensor memory) with token tiles of 64
-# or 128 rows, whose operands are fp16 (tokens rescaled per row) or, with
+# memory) or weights in M (widened into tensor memory) with token tiles of 32,
+# 64 or 128 rows, whose operands are fp16 (tokens rescaled per row) or, with
 # MOE_B300_FP8_TOKENS=bf16, bf16; shapes the weights-in-M kernel does not
 # support fall back to tokens in M
-FP8_LAYOUTS = ["tokens_m", "weights_tm", "weights_tm128", "weights_tm_bf16"]
+FP8_LAYOUTS = ["tokens_m", "weights_tm32", "weights_tm", "weights_tm128", "weights_tm_bf16",
+               "weights_tm32_bf16"]
 
 
 def _set_fp8_layout(monkeypatch, layout):

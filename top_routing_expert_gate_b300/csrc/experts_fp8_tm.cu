@@ -23,11 +23,11 @@
 // down: 256 rows of W_down) x up to TN tokens of one group (TN = 64 for small
 // batches, 128 for prefill; see TmTile), k-blocks of 128.
 //   warp 0      TMA producer of the E4M3 weight tiles (2 boxes of 128 rows x
-//               128 bytes, 128-byte swizzle) into a 5- or 4-slot ring;
-//   warp 1      allocates 512 TMEM columns; one thread issues, per k-block,
-//               16 tcgen05.mma (two halves x 8 K=16 steps) of M=128, N = the
-//               tile's tokens rounded up to 16, A from tensor memory, B (the
-//               tokens) from shared memory;
+//               128 bytes, 128-byte swizzle) into a 4- to 6-slot ring;
+//   warps 1, 3  warp 1 allocates 512 TMEM columns; one thread of each issues,
+//               per k-block, the 8 tcgen05.mma (K=16 steps) of its 128-row
+//               half: M=128, N = the tile's tokens rounded up to 16, A from
+//               tensor memory, B (the tokens) from shared memory;
 //   warp 2      TMA producer of the token tiles (valid rows only, rounded up
 //               to 16) into a 3- or 2-slot ring;
 //   warps 4..7, 16..19  epilogue, two warps per lane quarter: scales,
@@ -35,8 +35,8 @@
 //   warps 8..15 converters: warp (q, half) widens rows 32q..32q+31 of its
 //               half into tensor-memory lanes 32q..32q+31, 64 columns (128
 //               bf16 of K) per k-block.
-// Tensor memory: columns [0, 256) two widened-A stages of 128 columns
-// (half h at +64h); [256, 512) the accumulators, 2 x TN columns per buffer
+// Tensor memory: 128-column widened-A stages (three for 32-token tiles, else
+// two; half h at +64h), then the accumulators, 2 x TN columns per buffer
 // (half h at +TN·h, one column per token).
 //
 // fp16 operands (the default): the hardware widens two E4M3 codes to fp16x2
@@ -60,37 +60,44 @@ using namespace tc;
 
 constexpr int MBM = 128;                             // weight rows per half
 constexpr int MBK = 128;                             // K per k-block (codes per row)
-constexpr int MNT = 2;                               // widened-A stages in tensor memory
 constexpr uint32_t MF_HALF = MBM * MBK;              // 16 KB: 128 rows x 128 codes
 constexpr uint32_t MF_STAGE = 2 * MF_HALF;           // 32 KB
 constexpr int kMThreads = 640;
 constexpr int kMTokWarp = 2;
+constexpr int kMMma2Warp = 3;                       // issues the second half's MMAs
 constexpr int kMEpiWarp0 = 4;                       // and warps 16..19
 constexpr int kMConvWarp0 = 8;
 constexpr uint32_t kMTmemCols = 512;
-constexpr uint32_t kMAccCol0 = MNT * 128;            // first accumulator column
 constexpr int kMMaxGroups = kMaxExperts + 1;
-constexpr uint32_t kMCtrlBytes = 256 + 4 * (kMMaxGroups + 1 + 3 * kMMaxGroups);
+constexpr uint32_t kMBarBytes = 512;                 // barriers, TMEM address, abort flag
+constexpr uint32_t kMCtrlBytes = kMBarBytes + 4 * (kMMaxGroups + 1 + 3 * kMMaxGroups);
 constexpr int kMMaxBoxes = 4;
 
-// Token-tile width TN and what follows from it.  TN = 64 (small batches):
-// two accumulator buffers (the epilogue of one tile overlaps the next
-// tile's MMAs), 5 E4M3 and 3 token slots.  TN = 128 (prefill): the two
-// 128-column A stages and one 256-column accumulator fill tensor memory, so
-// the accumulator is single-buffered; 4 E4M3 and 2 token slots of 32 KB.
+// Token-tile width TN and what follows from it.  Tensor memory holds kNT
+// widened-A stages of 128 columns, then the accumulators (kNAcc buffers of
+// 2 x TN columns).
+//   TN = 32 (a few tokens per expert, as in decode): three A stages, so the
+//     converters run up to three k-blocks ahead of the MMAs, two
+//     accumulator buffers, 6 E4M3 and 3 token slots;
+//   TN = 64: two A stages, two accumulator buffers (the epilogue of one tile
+//     overlaps the next tile's MMAs), 5 E4M3 and 3 token slots;
+//   TN = 128 (prefill): two A stages and one 256-column accumulator, so the
+//     accumulator is single-buffered; 4 E4M3 and 2 token slots of 32 KB.
 template <int TN>
 struct TmTile {
   static constexpr int kTN = TN;
-  static constexpr int kNF = TN == 64 ? 5 : 4;       // E4M3 slots
-  static constexpr int kNA = TN == 64 ? 3 : 2;       // token slots
-  static constexpr int kNAcc = TN == 64 ? 2 : 1;     // accumulator buffers
-  static constexpr int kBoxes = TN == 64 ? 3 : 4;    // token boxes of TN, TN/2, .., 16 rows
+  static constexpr int kNT = TN == 32 ? 3 : 2;                    // widened-A stages
+  static constexpr int kNF = TN == 32 ? 6 : (TN == 64 ? 5 : 4);   // E4M3 slots
+  static constexpr int kNA = TN == 128 ? 2 : 3;                   // token slots
+  static constexpr int kNAcc = TN == 128 ? 1 : 2;                 // accumulator buffers
+  static constexpr int kBoxes = TN == 32 ? 2 : (TN == 64 ? 3 : 4);   // boxes of TN, TN/2, .., 16 rows
+  static constexpr uint32_t kAcc0 = kNT * 128;                    // first accumulator column
   static constexpr uint32_t kASub = TN * 128;        // TN token rows x 64 bf16
   static constexpr uint32_t kAStage = 2 * kASub;     // K = 128
   static constexpr uint32_t kSmem = kNF * MF_STAGE + kNA * kAStage + kMCtrlBytes + 1024;
-  static_assert(TN == 64 || TN == 128, "token tile of 64 or 128 rows");
+  static_assert(TN == 32 || TN == 64 || TN == 128, "token tile of 32, 64 or 128 rows");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
-  static_assert(kMAccCol0 + kNAcc * 2 * TN == kMTmemCols, "tensor memory budget");
+  static_assert(kAcc0 + kNAcc * 2 * TN == kMTmemCols, "tensor memory budget");
 };
 
 enum MMode { kMGateUp = 0, kMDown = 1 };
@@ -158,7 +165,8 @@ template <int MODE, int TN, bool F16>
 __global__ void __launch_bounds__(kMThreads, 1)
 grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
   using C = TmTile<TN>;
-  constexpr int MTN = C::kTN, MNF = C::kNF, MNA = C::kNA, NACC = C::kNAcc;
+  constexpr int MTN = C::kTN, MNF = C::kNF, MNA = C::kNA, NACC = C::kNAcc, MNT = C::kNT;
+  constexpr uint32_t kMAccCol0 = C::kAcc0;
   constexpr uint32_t MA_SUB = C::kASub, MA_STAGE = C::kAStage;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -170,7 +178,7 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
   uint8_t* ctrl = smem + MNF * MF_STAGE + MNA * MA_STAGE;
   const uint32_t bar0 = smem_u32(ctrl);
   // barriers: wfull[MNF], wempty[MNF], afull[MNA], aempty[MNA], tfull[MNT],
-  // tempty[MNT], accf[2], acce[2] (NACC used), drain
+  // tempty[MNT], accf[2], acce[2] (NACC used), drain[2]
   constexpr int kNB = 2 * MNF + 2 * MNA + 2 * MNT;
   auto wfull_bar = [&](int s) { return bar0 + 8u * s; };
   auto wempty_bar = [&](int s) { return bar0 + 8u * (MNF + s); };
@@ -180,11 +188,11 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
   auto tempty_bar = [&](int s) { return bar0 + 8u * (2 * MNF + 2 * MNA + MNT + s); };
   auto accf_bar = [&](int b) { return bar0 + 8u * (kNB + b); };
   auto acce_bar = [&](int b) { return bar0 + 8u * (kNB + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (kNB + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (kNB + 5));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 8 * (kNB + 5) + 4);
-  static_assert(8 * (kNB + 5) + 8 <= 256, "barriers fit the control header");
-  int* s_tile_start = reinterpret_cast<int*>(ctrl + 256);
+  auto drain_bar = [&](int h) { return bar0 + 8u * (kNB + 4 + h); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (kNB + 6));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 8 * (kNB + 6) + 4);
+  static_assert(8 * (kNB + 6) + 8 <= kMBarBytes, "barriers fit the control header");
+  int* s_tile_start = reinterpret_cast<int*>(ctrl + kMBarBytes);
   int* s_row0 = s_tile_start + (kMMaxGroups + 1);
   int* s_rows = s_row0 + kMMaxGroups;
   int* s_mtiles = s_rows + kMMaxGroups;
@@ -214,17 +222,18 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
     }
     for (int s = 0; s < MNA; ++s) {
       mbar_init(afull_bar(s), 1);
-      mbar_init(aempty_bar(s), 1);
+      mbar_init(aempty_bar(s), 2);    // one commit per MMA issuer
     }
     for (int s = 0; s < MNT; ++s) {
       mbar_init(tfull_bar(s), 8);
-      mbar_init(tempty_bar(s), 1);
+      mbar_init(tempty_bar(s), 2);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(accf_bar(b), 1);
+      mbar_init(accf_bar(b), 2);
       mbar_init(acce_bar(b), 8);      // one arrival per epilogue warp
     }
-    mbar_init(drain_bar, 1);
+    mbar_init(drain_bar(0), 1);
+    mbar_init(drain_bar(1), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -320,9 +329,12 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == kMMma2Warp) {
     if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+      // ---------------- MMA issuers: warp 1 the first 128-row half, warp 3
+      // the second (each MMA instruction takes its issuing thread tens of
+      // cycles, and a small token tile makes sixteen per k-block) ----------
+      const int hm = warp == 1 ? 0 : 1;
       int i = 0, local = 0;
       for (int t = blockIdx.x; t < total && !failed; t += gridDim.x, ++local) {
         int g, m, n;
@@ -354,9 +366,8 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
                 sdesc_k128(sA + as * MA_STAGE + (uint32_t)(kk >> 2) * MA_SUB) +
                 (uint64_t)(2 * (kk & 3));
             const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-            mma_bf16_ta(d_tmem, a_tmem + (uint32_t)(8 * kk), b_desc, idesc, acc);
-            mma_bf16_ta(d_tmem + (uint32_t)MTN, a_tmem + 64u + (uint32_t)(8 * kk), b_desc, idesc,
-                        acc);
+            mma_bf16_ta(d_tmem + (uint32_t)(hm * MTN), a_tmem + (uint32_t)(hm * 64 + 8 * kk),
+                        b_desc, idesc, acc);
           }
           mma_commit(aempty_bar(as));
           mma_commit(tempty_bar(ts));
@@ -367,8 +378,8 @@ grouped_gemm_fp8_tm_kernel(const __grid_constant__ MParams p) {
       if (failed) {
         *abort_flag = 1;
         record_error(p.status, kDevTimeout);
-        mma_commit(drain_bar);
-        mbar_wait(drain_bar, 0, nullptr, p.timeout_ns);
+        mma_commit(drain_bar(hm));
+        mbar_wait(drain_bar(hm), 0, nullptr, p.timeout_ns);
       }
     }
   } else if (warp == kMTokWarp) {
@@ -676,7 +687,7 @@ cudaError_t launch_rows_to_f16(const void* in, void* out, float* scale, int rows
 cudaError_t launch_gemm_fp8_tm(const moe_config_t& c, const ExpertArgs& a, int which, int tn,
                                cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
-  if (!fp8_tm_supported(c) || (tn != 64 && tn != 128)) return cudaErrorInvalidValue;
+  if (!fp8_tm_supported(c) || (tn != 32 && tn != 64 && tn != 128)) return cudaErrorInvalidValue;
   const bool f16 = a.tok_scale != nullptr;
   const int T = c.T, E = c.n_experts, d = c.d_model, F = c.d_ff, Fs = c.d_ff_shared;
   const int A = a.rows > 0 ? a.rows : T * c.top_k;
@@ -755,12 +766,16 @@ cudaError_t launch_gemm_fp8_tm(const moe_config_t& c, const ExpertArgs& a, int w
   cudaError_t err;
   const bool up = which == kGemmGateUp;
   if (f16) {
-    if (tn == 64)
+    if (tn == 32)
+      err = up ? launch_m<kMGateUp, 32, true>(p, s) : launch_m<kMDown, 32, true>(p, s);
+    else if (tn == 64)
       err = up ? launch_m<kMGateUp, 64, true>(p, s) : launch_m<kMDown, 64, true>(p, s);
     else
       err = up ? launch_m<kMGateUp, 128, true>(p, s) : launch_m<kMDown, 128, true>(p, s);
   } else {
-    if (tn == 64)
+    if (tn == 32)
+      err = up ? launch_m<kMGateUp, 32, false>(p, s) : launch_m<kMDown, 32, false>(p, s);
+    else if (tn == 64)
       err = up ? launch_m<kMGateUp, 64, false>(p, s) : launch_m<kMDown, 64, false>(p, s);
     else
       err = up ? launch_m<kMGateUp, 128, false>(p, s) : launch_m<kMDown, 128, false>(p, s);

@@ -176,19 +176,25 @@ bool weights_in_m(const moe_config_t& c, int which) {
 }
 
 // E4M3 GEMM layout: the token-tile width of the weights-in-M kernel that
-// widens into tensor memory (launch_gemm_fp8_tm: 64 for batches of a few
-// tokens per expert, 128 for larger ones), or 0 for tokens in M
-// (launch_gemm_fp8w).  The default takes 64 when the average expert gets at
-// most 64 rows and the shared expert at most 256, else 128;
-// MOE_B300_FP8_LAYOUT=tokens_m|weights_tm|weights_tm128 overrides it for
-// tests and tuning.
+// widens into tensor memory (launch_gemm_fp8_tm: 32 or 64 for batches of a
+// few tokens per expert, 128 for larger ones), or 0 for tokens in M
+// (launch_gemm_fp8w).  The default takes 32 when the average expert gets at
+// most 8 rows and the shared expert at most 64 (decode: every weight tile
+// is streamed once, and the deeper widened-A ring keeps the MMAs off the
+// critical path), 64 when the average expert gets at most 64 rows and the
+// shared expert at most 256, else 128;
+// MOE_B300_FP8_LAYOUT=tokens_m|weights_tm32|weights_tm|weights_tm128
+// overrides it for tests and tuning.
 int fp8_tmem_tile(const moe_config_t& c) {
   if (!fp8_tm_supported(c)) return 0;
   const char* o = getenv("MOE_B300_FP8_LAYOUT");
   if (o && strcmp(o, "tokens_m") == 0) return 0;
+  if (o && strcmp(o, "weights_tm32") == 0) return 32;
   if (o && strcmp(o, "weights_tm") == 0) return 64;
   if (o && strcmp(o, "weights_tm128") == 0) return 128;
-  return (int64_t)c.T * c.top_k <= (int64_t)64 * c.n_experts && c.T <= 256 ? 64 : 128;
+  const int64_t A = (int64_t)c.T * c.top_k;
+  if (A <= (int64_t)8 * c.n_experts && c.T <= 64) return 32;
+  return A <= (int64_t)64 * c.n_experts && c.T <= 256 ? 64 : 128;
 }
 
 // The gather (x_perm[r] = x[perm[r] / div]) and the two grouped GEMMs.  With
