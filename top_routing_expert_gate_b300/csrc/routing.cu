@@ -370,13 +370,37 @@ balance_loss_kernel(const int32_t* __restrict__ counts, const int32_t* __restric
   }
 }
 
-__global__ void mean_prob_finalize_kernel(const float* __restrict__ mp_partial, int nblocks,
-                                          int E, int T, float* __restrict__ mean_prob) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= E) return;
+// mean_prob[e] = (sum over the top-k blocks' partials) / T.  One block per
+// 32 experts: warp w adds the partials of blocks w, w + 32, ... for expert
+// e0 + lane (eight loads in flight), then lane e of warp 0 adds the 32 warp
+// sums in warp order, a fixed order whatever the timing.
+constexpr int kFinalizeWarps = 32;
+__global__ void __launch_bounds__(kFinalizeWarps * 32)
+mean_prob_finalize_kernel(const float* __restrict__ mp_partial, int nblocks, int E, int T,
+                          float* __restrict__ mean_prob) {
+  __shared__ float ws[kFinalizeWarps][33];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + lane;
   float s = 0.f;
-  for (int b = 0; b < nblocks; ++b) s += mp_partial[(size_t)b * E + e];
-  mean_prob[e] = T > 0 ? s / (float)T : 0.f;
+  if (e < E) {
+    int b = warp;
+    for (; b + 7 * kFinalizeWarps < nblocks; b += 8 * kFinalizeWarps) {
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = mp_partial[(size_t)(b + i * kFinalizeWarps) * E + e];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s += v[i];
+    }
+    for (; b < nblocks; b += kFinalizeWarps) s += mp_partial[(size_t)b * E + e];
+  }
+  ws[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && e < E) {
+    float t = 0.f;
+#pragma unroll 8
+    for (int w = 0; w < kFinalizeWarps; ++w) t += ws[w][lane];
+    mean_prob[e] = T > 0 ? t / (float)T : 0.f;
+  }
 }
 
 }  // namespace
@@ -408,7 +432,8 @@ cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_ro
 
 cudaError_t launch_mean_prob_finalize(const float* mp_partial, int nblocks, int E, int T,
                                       float* mean_prob, cudaStream_t s, LaunchCounter* lc) {
-  mean_prob_finalize_kernel<<<(E + 255) / 256, 256, 0, s>>>(mp_partial, nblocks, E, T, mean_prob);
+  mean_prob_finalize_kernel<<<(E + 31) / 32, kFinalizeWarps * 32, 0, s>>>(mp_partial, nblocks,
+                                                                          E, T, mean_prob);
   count_launch(lc);
   return cudaGetLastError();
 }
@@ -484,7 +509,8 @@ cudaError_t launch_topk(const moe_config_t& c, const LogitsView& z, const float*
   count_launch(lc);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || !mean_prob) return err;
-  mean_prob_finalize_kernel<<<(E + 255) / 256, 256, 0, s>>>(mp_partial, nblocks, E, T, mean_prob);
+  mean_prob_finalize_kernel<<<(E + 31) / 32, kFinalizeWarps * 32, 0, s>>>(mp_partial, nblocks,
+                                                                          E, T, mean_prob);
   count_launch(lc);
   return cudaGetLastError();
 }
