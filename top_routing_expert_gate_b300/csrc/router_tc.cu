@@ -7,7 +7,9 @@
 // few token tiles.  Each split writes its own fp32 partial [T, E]; the top-k
 // kernel adds the partials in split order, so the logits are deterministic.
 //   warp 0      TMA producer: 128x64 x tile + E_pad x 64 W_router tile per
-//               k-block (128-byte swizzle) into a 4-stage ring;
+//               k-block (128-byte swizzle) into a ring of as many stages as
+//               192 KB holds (4 for 256 experts, 8 for 64 or fewer), so that a
+//               small expert count still keeps ~192 KB of loads in flight;
 //   warp 1      allocates the accumulator's TMEM columns; one thread issues
 //               tcgen05.mma M=128 N=E_pad K=16;
 //   warps 2..5  epilogue: tcgen05.ld of its 32 TMEM lanes, stored as row
@@ -23,9 +25,10 @@ using namespace tc;
 
 constexpr int BM = 128;            // tokens per tile
 constexpr int BK = 64;             // one 128-byte swizzle span of bf16
-constexpr int STAGES = 4;
+constexpr int kMaxStages = 8;
+constexpr uint32_t kRingBytes = 192 * 1024;   // the stage ring, whatever the stage size
 constexpr uint32_t A_STAGE = BM * BK * 2;   // 16 KB
-constexpr uint32_t B_STAGE = kMaxExperts * BK * 2;   // 32 KB: every expert row
+static_assert(2 * (A_STAGE + kMaxExperts * BK * 2) <= kRingBytes, "two stages of the widest weight tile");
 constexpr int kThreads = 192;
 
 struct RouterParams {
@@ -33,12 +36,13 @@ struct RouterParams {
   CUtensorMap b_map;   // W_router [E, d], box 64 x E_pad
   float* partial;      // [splits, T, E]
   int T, E, E_pad, kb_total, kb_per, m_tiles;
+  int stages;          // ring depth: as many stages as kRingBytes holds, 2..kMaxStages
   uint32_t tmem_cols;
   int32_t* status;
   uint64_t timeout_ns;
 };
 
-constexpr uint32_t kRouterSmemMax = STAGES * (A_STAGE + B_STAGE) + 256 + 1024;
+constexpr uint32_t kRouterSmemMax = kRingBytes + 256 + 1024;
 
 __global__ void __launch_bounds__(kThreads, 1)
 router_gemm_kernel(const __grid_constant__ RouterParams p) {
@@ -48,6 +52,7 @@ router_gemm_kernel(const __grid_constant__ RouterParams p) {
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t b_stage = (uint32_t)p.E_pad * 128u;
   const uint32_t sA = base;
+  const int STAGES = p.stages;
   const uint32_t sB = base + STAGES * A_STAGE;
   uint8_t* ctrl = smem + STAGES * (A_STAGE + b_stage);
   const uint32_t bar0 = smem_u32(ctrl);
@@ -228,8 +233,15 @@ cudaError_t launch_router_tc(const moe_config_t& c, const void* x, const void* w
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kRouterSmemMax);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const uint32_t smem = STAGES * (A_STAGE + (uint32_t)p.E_pad * 128u) + 256 + 1024;
-  router_gemm_kernel<<<plan.m_tiles * plan.splits, kThreads, smem, s>>>(p);
+  // a few experts make small stages: keep ~192 KB of loads in flight per
+  // SM, split among the CTAs an SM must hold for the grid to run in one wave
+  const int ctas = plan.m_tiles * plan.splits;
+  const int per_sm = (ctas + num_sms() - 1) / num_sms();
+  const uint32_t stage_bytes = A_STAGE + (uint32_t)p.E_pad * 128u;
+  int stages = (int)(kRingBytes / (uint32_t)per_sm / stage_bytes);
+  p.stages = stages < 2 ? 2 : (stages > kMaxStages ? kMaxStages : stages);
+  const uint32_t smem = (uint32_t)p.stages * stage_bytes + 256 + 1024;
+  router_gemm_kernel<<<ctas, kThreads, smem, s>>>(p);
   count_launch(lc);
   return cudaGetLastError();
 }
