@@ -141,20 +141,64 @@ def stored_traffic(workload: str, stage: str):
     return rec.get("dram_bytes_per_launch")
 
 
+# Polls one GPU through NVML, the driver's management library, called with
+# ctypes (read-only queries: SM clock, its maximum, the active clock-event
+# reasons), and prints "host_time sm_mhz max_mhz reason_mask" per sample until
+# it is terminated.  A process of its own, so that the bench's Python thread
+# holding the interpreter lock cannot delay the samples.
+_NVML_POLL_SRC = r"""
+import ctypes, sys, time
+nv = ctypes.CDLL("libnvidia-ml.so.1")
+if nv.nvmlInit_v2() != 0:
+    sys.exit(1)
+h = ctypes.c_void_p()
+if nv.nvmlDeviceGetHandleByPciBusId_v2(sys.argv[1].encode(), ctypes.byref(h)) != 0:
+    sys.exit(1)
+period = float(sys.argv[2])
+try:
+    reasons = nv.nvmlDeviceGetCurrentClocksEventReasons
+except AttributeError:
+    reasons = nv.nvmlDeviceGetCurrentClocksThrottleReasons
+SM = 1   # NVML_CLOCK_SM
+clk, mx, mask = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+if nv.nvmlDeviceGetMaxClockInfo(h, SM, ctypes.byref(mx)) != 0:
+    sys.exit(1)
+out = sys.stdout
+while True:
+    t = time.time()
+    if nv.nvmlDeviceGetClockInfo(h, SM, ctypes.byref(clk)) != 0 or \
+            reasons(h, ctypes.byref(mask)) != 0:
+        sys.exit(1)
+    out.write("%.6f %d %d %d\n" % (t, clk.value, mx.value, mask.value))
+    out.flush()
+    time.sleep(period)
+"""
+
+
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 50 ms; only the
-    samples taken inside the timed window (mark_begin .. mark_end, host wall
-    clock) enter the summary."""
+    """SM clock and clock-event reasons sampled during the timed window.
+
+    A child process polls NVML every 5 ms (read-only queries), so that even a
+    20 ms window holds a few samples; `nvidia-smi -lms 50` stands in when
+    the NVML library cannot be loaded.  Only the samples taken inside the timed window
+    (mark_begin .. mark_end, host wall clock) enter the summary.  Nothing
+    here changes a GPU setting."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    # NVML clock-event reason bits of the four reasons above
+    REASON_BITS = (0x8, 0x40, 0x20, 0x4)
+    PERIOD_S = 0.005
 
     def __init__(self, device_index: int):
         self.proc = None
         self.lines = []
+        self.nvml_lines = []
         self.dev = device_index
         self.t0 = self.t1 = None
+        self.source = None
 
     def mark_begin(self):
         self.t0 = time.time()
@@ -172,11 +216,26 @@ class ClockSampler:
             return vis.split(",")[self.dev] if vis else str(self.dev)
 
     def start(self):
+        # the NVML poller, once it has taken its first sample; else nvidia-smi
+        try:
+            self.proc = subprocess.Popen(
+                [sys.executable, "-c", _NVML_POLL_SRC, self._smi_id(), str(self.PERIOD_S)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            first = self.proc.stdout.readline()
+            if first.strip():
+                self.nvml_lines = [first]
+                self.source = "nvml"
+                return
+            self.proc.wait(timeout=5)
+        except (OSError, subprocess.TimeoutExpired):
+            pass
+        self.proc = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "50", "-i", self._smi_id()],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
         except OSError:
             self.proc = None
 
@@ -189,7 +248,11 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        lines = [ln for ln in out.splitlines() if ln.strip()]
+        if self.source == "nvml":
+            self.nvml_lines += lines
+        else:
+            self.lines = lines
 
     @staticmethod
     def _stamp(text):
@@ -199,16 +262,28 @@ class ClockSampler:
         except ValueError:
             return None
 
+    def _in_window(self, ts):
+        return ts is None or self.t0 is None or self.t1 is None or self.t0 <= ts <= self.t1
+
     def summary(self):
         sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.nvml_lines:
+            parts = ln.split()
+            try:
+                ts, mhz, top, mask = float(parts[0]), float(parts[1]), float(parts[2]), int(parts[3])
+            except (ValueError, IndexError):
+                continue
+            if not self._in_window(ts):
+                continue
+            sm.append(mhz)
+            mx = top
+            reasons |= {n for n, b in zip(self.REASONS, self.REASON_BITS) if mask & b}
+        names = list(self.REASONS)
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 10:
                 continue
-            ts = self._stamp(parts[0])
-            if ts is not None and self.t0 is not None and self.t1 is not None and \
-                    not (self.t0 <= ts <= self.t1):
+            if not self._in_window(self._stamp(parts[0])):
                 continue
             try:
                 sm.append(float(parts[2]))

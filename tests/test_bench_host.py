@@ -95,3 +95,21 @@ def test_committed_traffic_records_name_their_capture():
             assert rec["dram_bytes_per_launch"] > 0
             assert bench.os.path.exists(bench.os.path.join(
                 bench.ROOT, "profiles", rec["capture"].split(" ")[0]))
+
+
+def test_clock_sampler_counts_only_the_timed_window():
+    # NVML poller lines "host_time sm_mhz max_mhz reason_mask": two before the
+    # window, three inside (one under the software power cap, bit 0x4, and an
+    # unreported reason bit 0x1), one after
+    cs = bench.ClockSampler(0)
+    cs.source = "nvml"
+    cs.t0, cs.t1 = 100.0, 100.02
+    cs.nvml_lines = ["99.990 2032 2032 0", "99.995 2032 2032 0",
+                     "100.000 1980 2032 5", "100.010 1200 2032 0", "100.020 1300 2032 1",
+                     "100.030 2032 2032 4", "garbled"]
+    s = cs.summary()
+    assert s["samples"] == 3
+    assert s["sm_mhz"] == 1300.0 and s["sm_max_mhz"] == 2032.0
+    assert s["reasons"] == ["sw_power_cap"]
+    assert tuple(bench.ClockSampler.REASONS) == ("hw_slowdown", "hw_thermal_slowdown",
+                                                 "sw_thermal_slowdown", "sw_power_cap")
