@@ -53,7 +53,6 @@ constexpr int BN = 256;            // MMA N (gate/up: 128 gate + 128 up columns)
 constexpr int STAGES = 4;
 constexpr uint32_t A_STAGE = BM * BK * 2;   // 16 KB
 constexpr uint32_t B_STAGE = BN * BK * 2;   // 32 KB
-constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxGroups = kMaxExperts + 1;
@@ -68,7 +67,8 @@ constexpr uint32_t kSmemBytes = STAGES * (A_STAGE + B_STAGE) + kEpiBytes + kCtrl
 enum Mode { kGateUp = 0, kDown = 1 };
 
 struct TcParams {
-  CUtensorMap a_map[2];   // [0] routed grouped rows, [1] shared-expert rows
+  CUtensorMap a_map[2];   // [0] routed grouped rows, [1] shared-expert rows (128-row box)
+  CUtensorMap a_part[2][3];   // the same rows in boxes of 64, 32 and 16 (partial tiles)
   CUtensorMap b_map[2];   // gate (kGateUp) or down (kDown) weights
   CUtensorMap u_map[2];   // up weights (kGateUp only)
   const int32_t* offsets; // [E + 1]
@@ -199,16 +199,36 @@ grouped_gemm_kernel(const __grid_constant__ TcParams p) {
         const int nk = p.K[kind] / BK;
         const int a_row = s_row0[g] + m * BM;
         const int b_row = (kind ? 0 : g * p.b_rows_per_expert) + n * (MODE == kGateUp ? 128 : BN);
+        // a partial tile run transposed reads only its token rows, rounded
+        // up to 16 (the MMA's N)
+        const int valid = min(BM, s_rows[g] - m * BM);
+        const int n_load = valid < BM && p.transpose_partial ? (valid + 15) & ~15 : BM;
+        const uint32_t tx = (uint32_t)n_load * (BK * 2) + B_STAGE;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
             failed = true;
             break;
           }
           const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, STAGE_TX);
+          mbar_arrive_expect_tx(fb, tx);
           const uint32_t a_dst = sA + stage * A_STAGE;
           const uint32_t b_dst = sB + stage * B_STAGE;
-          tma_load_2d(a_dst, &p.a_map[kind], fb, kb * BK, a_row);
+          if (n_load == BM) {
+            tma_load_2d(a_dst, &p.a_map[kind], fb, kb * BK, a_row);
+          } else {
+            // boxes of 64, 32, 16 rows, each starting on a 16-row (2 KB)
+            // boundary of the stage, so the swizzle pattern is the full tile's
+            int off = 0;
+#pragma unroll
+            for (int b = 0; b < 3; ++b) {
+              const int box = 64 >> b;
+              while (n_load - off >= box) {
+                tma_load_2d(a_dst + (uint32_t)off * (BK * 2), &p.a_part[kind][b], fb, kb * BK,
+                            a_row + off);
+                off += box;
+              }
+            }
+          }
           if (MODE == kGateUp) {
             tma_load_2d(b_dst, &p.b_map[kind], fb, kb * BK, b_row);
             tma_load_2d(b_dst + B_STAGE / 2, &p.u_map[kind], fb, kb * BK, b_row);
@@ -456,6 +476,13 @@ cudaError_t launch(const TcParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Token rows in boxes of 64, 32 and 16 rows, for partial tiles.
+bool part_maps(CUtensorMap (&m)[3], const void* ptr, uint64_t inner, uint64_t rows) {
+  bool ok = true;
+  for (int b = 0; b < 3; ++b) ok &= make_map(&m[b], ptr, inner, rows, 64u >> b);
+  return ok;
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_tc(const moe_config_t& c, const ExpertArgs& a, int which,
@@ -469,6 +496,8 @@ cudaError_t launch_gemm_tc(const moe_config_t& c, const ExpertArgs& a, int which
   bool ok = true;
   ok &= make_map(&p1.a_map[0], a.x_perm, d, A, BM);
   ok &= make_map(&p1.a_map[1], a.x, d, T, BM);
+  ok &= part_maps(p1.a_part[0], a.x_perm, d, A);
+  ok &= part_maps(p1.a_part[1], a.x, d, T);
   ok &= make_map(&p1.b_map[0], a.w_gate, d, (uint64_t)E * F, 128);
   ok &= make_map(&p1.u_map[0], a.w_up, d, (uint64_t)E * F, 128);
   if (has_shared) {
@@ -503,12 +532,15 @@ cudaError_t launch_gemm_tc(const moe_config_t& c, const ExpertArgs& a, int which
   TcParams p2 = p1;
   ok = true;
   ok &= make_map(&p2.a_map[0], a.h, F, A, BM);
+  ok &= part_maps(p2.a_part[0], a.h, F, A);
   ok &= make_map(&p2.b_map[0], a.w_down, F, (uint64_t)E * d, BN);
   if (has_shared) {
     ok &= make_map(&p2.a_map[1], a.h_shared, Fs, T, BM);
+    ok &= part_maps(p2.a_part[1], a.h_shared, Fs, T);
     ok &= make_map(&p2.b_map[1], a.ws_down, Fs, d, BN);
   } else {
     p2.a_map[1] = p2.a_map[0];
+    for (int b = 0; b < 3; ++b) p2.a_part[1][b] = p2.a_part[0][b];
     p2.b_map[1] = p2.b_map[0];
   }
   if (!ok) return cudaErrorInvalidValue;
