@@ -524,9 +524,12 @@ def layer_rates(work, ms_per_step, peaks, tensor_key):
 
 
 def measure_workload(name, args, dev, world, rank, peaks, peak_src, oracle_cache):
-    """One workload on this rank: warm-up, K timed steps, the sustained loop,
-    the end-to-end leg and (rank 0, one GPU) the oracle baseline.  Returns the
-    record rank 0 reports (None on other ranks)."""
+    """One workload on this rank: warm-up, K timed steps, the sustained loop
+    and the end-to-end leg.  Returns the record rank 0 reports (None on other
+    ranks) and, on rank 0 of a one-GPU run, a function that times the oracle
+    baseline on the host and adds it to the record: main calls those after
+    every GPU measurement, so that the GPU does not sit idle (and clock down)
+    between one workload's timed steps and the next one's."""
     import torch
     import torch.distributed as dist
 
@@ -686,11 +689,13 @@ def measure_workload(name, args, dev, world, rank, peaks, peak_src, oracle_cache
                              "(L2 126 MB)",
                        "kept_assignments": work["kept"], "touched_experts": work["touched"]},
         }
-        if world == 1 and not args.no_cpu_baseline:
+    cpu_job = None
+    if record is not None and world == 1 and not args.no_cpu_baseline:
+        def cpu_job(rec=record, shape=shape, inputs=inputs):
             samples = oracle_samples(shape, args.cpu_sample_tokens, args.cpu_steps)
             times, used = timed_oracle(shape, inputs, samples, cache=oracle_cache)
             t = statistics.mean(times)
-            record["cpu_baseline"] = {
+            rec["cpu_baseline"] = {
                 "value": len(samples[0]) / t, "unit": "tokens/s", "cores": used,
                 "kind": "oracle",
                 "sample": f"{args.cpu_steps} oracle steps, each: routing of all {T} tokens + "
@@ -699,12 +704,14 @@ def measure_workload(name, args, dev, world, rank, peaks, peak_src, oracle_cache
             if name == "tiny":
                 # the small layer's single-thread figure beside the all-core one
                 times1, _ = timed_oracle(shape, inputs, samples, threads=1, cache=oracle_cache)
-                record["cpu_baseline"]["single_thread_value"] = (len(samples[0]) /
-                                                                 statistics.mean(times1))
-    del pipes, inputs, w, ws, x, y
+                rec["cpu_baseline"]["single_thread_value"] = (len(samples[0]) /
+                                                              statistics.mean(times1))
+    del pipes, w, ws, x, y
+    if cpu_job is None:
+        del inputs
     torch.cuda.synchronize(dev)
     torch.cuda.empty_cache()
-    return record
+    return record, cpu_job
 
 
 def reference_main(args, rank, local_rank):
@@ -762,9 +769,15 @@ def main(argv=None):
     for n in names:
         if n not in WORKLOAD_TEXT:
             raise SystemExit(f"unknown workload {n!r}")
-    records = {}
+    records, cpu_jobs = {}, []
     for n in names:
-        records[n] = measure_workload(n, args, dev, world, rank, peaks, peak_src, cache)
+        records[n], job = measure_workload(n, args, dev, world, rank, peaks, peak_src, cache)
+        if job is not None:
+            cpu_jobs.append(job)
+    # the host-side oracle baselines, once the GPU measurements are done
+    for job in cpu_jobs:
+        job()
+    del cpu_jobs
 
     if rank == 0:
         head = records[args.workload]
