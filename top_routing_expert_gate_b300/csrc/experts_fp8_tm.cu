@@ -20,8 +20,8 @@
 // costs MMA time in proportion to its rows (N rounded up to 16).
 //
 // Tile: 256 weight rows (gate/up: 128 W_gate rows and the same 128 W_up rows;
-// down: 256 rows of W_down) x up to TN tokens of one group (TN = 64 for small
-// batches, 128 for prefill; see TmTile), k-blocks of 128.
+// down: 256 rows of W_down) x up to TN tokens of one group (TN = 32 or 64 for
+// small batches, 128 for prefill; see TmTile), k-blocks of 128.
 //   warp 0      TMA producer of the E4M3 weight tiles (2 boxes of 128 rows x
 //               128 bytes, 128-byte swizzle) into a 4- to 6-slot ring;
 //   warps 1, 3  warp 1 allocates 512 TMEM columns; one thread of each issues,
