@@ -113,3 +113,18 @@ def test_clock_sampler_counts_only_the_timed_window():
     assert s["reasons"] == ["sw_power_cap"]
     assert tuple(bench.ClockSampler.REASONS) == ("hw_slowdown", "hw_thermal_slowdown",
                                                  "sw_thermal_slowdown", "sw_power_cap")
+
+
+def test_clock_sampler_without_a_gpu_reports_no_samples():
+    # no NVML library and no nvidia-smi here: the sampler must neither raise
+    # nor invent samples
+    cs = bench.ClockSampler(0)
+    cs.start()
+    cs.mark_begin()
+    cs.mark_end()
+    cs.stop()
+    s = cs.summary()
+    if cs.source is None:
+        assert s == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    else:   # a machine with a GPU: whatever it sampled lies inside the window
+        assert s["samples"] >= 0
